@@ -1,0 +1,157 @@
+/*
+ * addln.h - C ABI of the GB300 (sm_103a) fused residual-Add + LayerNorm library.
+ *
+ * The operation, per row i of the row-major [rows, H] inputs X and R:
+ *     A_i    = X_i + R_i                         residual add; A never goes to memory
+ *                                                 unless the caller asks for it
+ *     mean_i = (1/H) sum_j A_ij
+ *     var_i  = (1/H) sum_j (A_ij - mean_i)^2     biased variance
+ *     rstd_i = 1 / sqrt(var_i + eps)
+ *     Y_ij   = gamma_j * (A_ij - mean_i) * rstd_i + beta_j
+ * Sources: the residual-Add + LayerNorm subgraph and its fused traffic (read X
+ * and R once, write Y once) are from "算子融合的收益量化" (fusion gains
+ * quantified), section 1; the LayerNorm definition (two-pass mean/variance,
+ * biased variance, eps inside the square root, per-element gamma and beta) is
+ * fused_layernorm in "算子融合与Kernel合并" (operator fusion and kernel
+ * merging), section 4.2; the optional extra outputs are that page's
+ * multi-output pattern (section 4.4 table).
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers to tensors are caller-owned DEVICE pointers (cudaMalloc or any
+ *    allocator, e.g. PyTorch's).  The library never allocates, frees or
+ *    synchronises inside the compute calls; it only enqueues kernels.
+ *  - Layout: X, R, Y, A are contiguous row-major [rows, H] (row stride H) in
+ *    the I/O dtype; gamma, beta are fp32 [H]; mean, rstd are fp32 [rows].
+ *  - dtype: ADDLN_FP32, ADDLN_FP16 or ADDLN_BF16 (IEEE binary32, binary16,
+ *    bfloat16).  Arithmetic is fp32 in registers; Y and A are rounded to the
+ *    I/O dtype to nearest-even.
+ *  - stream: a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Work is asynchronous: a zero return means the arguments were
+ *    valid and the launch was accepted, not that the kernel finished.
+ *  - Misaligned pointers or an H that is not a whole number of 16-byte
+ *    vectors are accepted; they select a slower element-wise path.
+ *  - Aliasing: an output may be exactly the same buffer as X or R (same base
+ *    pointer, in-place); every row is read in full before any of its outputs
+ *    is written.  Any other overlap between an output and any input or other
+ *    output returns ADDLN_ERR_ALIAS.
+ *  - Errors are negative return codes; nothing aborts or exits.  All argument
+ *    checks run before the first CUDA call, so a rejected call touches no
+ *    device state.
+ *  - rows == 0 is a successful no-op once dtype, H and eps are valid.
+ *  - Thread safety: every entry point may be called from several host threads
+ *    at once; addln_set_force_path and addln_set_wait_limit_ns change
+ *    process-wide test settings.
+ */
+#ifndef ADDLN_H
+#define ADDLN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype codes */
+#define ADDLN_FP32 0
+#define ADDLN_FP16 1
+#define ADDLN_BF16 2
+
+/* return codes */
+#define ADDLN_OK 0
+#define ADDLN_ERR_NULL (-1)           /* a required pointer is NULL */
+#define ADDLN_ERR_SHAPE (-2)          /* rows < 0, n < 0, H <= 0 or H > addln_max_hidden(dtype) */
+#define ADDLN_ERR_DTYPE (-3)          /* unknown dtype code */
+#define ADDLN_ERR_EPS (-4)            /* eps negative, NaN or infinite */
+#define ADDLN_ERR_ALIAS (-5)          /* an output partially overlaps an input or another output */
+#define ADDLN_ERR_LAUNCH (-6)         /* the CUDA launch failed (cudaGetLastError) */
+#define ADDLN_ERR_UNSUPPORTED (-7)    /* a forced kernel path cannot run these arguments */
+#define ADDLN_ERR_DEVICE_TIMEOUT (-8) /* a kernel's bounded wait on its own copy ran out */
+#define ADDLN_ERR_CUDA (-9)           /* a CUDA runtime call outside a launch failed */
+
+/* kernel paths for addln_set_force_path */
+#define ADDLN_PATH_AUTO 0
+#define ADDLN_PATH_WARP_VEC 1   /* one warp per row, 16-byte vector loads, H <= 1024 */
+#define ADDLN_PATH_CTA_TMA 2    /* one CTA per row, rows staged by TMA bulk copies */
+#define ADDLN_PATH_CTA_VEC 3    /* one CTA per row, 16-byte vector loads */
+#define ADDLN_PATH_SCALAR 4     /* element-wise loads; any alignment and H */
+
+/*
+ * Fused residual-Add + LayerNorm forward (definition above).
+ *   x, r        [rows, H] inputs in dtype (required)
+ *   gamma, beta [H] fp32 (required)
+ *   y           [rows, H] output in dtype (required)
+ *   resid_out   [rows, H] output A = X + R rounded to dtype, or NULL
+ *   mean, rstd  [rows] fp32 outputs, each independently NULL-able
+ *   eps         >= 0, added to the variance inside the square root
+ * Statistics use the unrounded fp32 sum, not A rounded to dtype.
+ * Returns ADDLN_OK or a negative code.
+ */
+int add_layernorm_fwd(const void *x, const void *r, const float *gamma, const float *beta,
+                      void *y, void *resid_out, float *mean, float *rstd,
+                      int64_t rows, int64_t H, float eps, int dtype, void *stream);
+
+/*
+ * Unfused baseline, step 1: A = X + R rounded to dtype, elementwise over n
+ * contiguous elements ("算子融合的收益量化" section 1, the separate Residual
+ * Add kernel: two reads, one write).  a may equal x or r exactly.
+ */
+int add_fwd(const void *x, const void *r, void *a, int64_t n, int dtype, void *stream);
+
+/*
+ * Unfused baseline, step 2: LayerNorm of the stored A ("算子融合与Kernel合并"
+ * 4.2 applied to the [rows, H] tensor a).  Same contract as add_layernorm_fwd
+ * without R; mean and rstd may be NULL.  y may equal a exactly.
+ */
+int layernorm_fwd(const void *a, const float *gamma, const float *beta, void *y, float *mean,
+                  float *rstd, int64_t rows, int64_t H, float eps, int dtype, void *stream);
+
+/* Static text for a return code (never NULL). */
+const char *addln_strerror(int code);
+
+/* Largest H accepted for dtype (32768 for 16-bit types, 16384 for fp32), or
+ * ADDLN_ERR_DTYPE. */
+int64_t addln_max_hidden(int dtype);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word, which a kernel sets when a bounded wait on its own TMA copy runs out.
+ * Returns ADDLN_OK, ADDLN_ERR_DEVICE_TIMEOUT, or ADDLN_ERR_CUDA if the
+ * synchronisation or the read failed.  Rows of a kernel that timed out are
+ * left unwritten.
+ */
+int addln_get_device_error(void *stream);
+
+/*
+ * Test and benchmark only.  Forces the kernel path of add_layernorm_fwd and
+ * layernorm_fwd (ADDLN_PATH_*); ADDLN_PATH_AUTO restores the dispatcher.  A
+ * forced path that cannot run a call's arguments makes that call return
+ * ADDLN_ERR_UNSUPPORTED.  Returns the previous setting, or ADDLN_ERR_SHAPE
+ * for an unknown path.
+ */
+int addln_set_force_path(int path);
+
+/*
+ * Test only.  Sets the bound, in nanoseconds, of the waits on in-flight TMA
+ * copies (default 1e9).  0 makes every such wait give up at once, which
+ * exercises the timeout path without any hang: the kernel records
+ * ADDLN_ERR_DEVICE_TIMEOUT, waits (again bounded, 1 s) for its copies to
+ * land, and returns.  Returns the previous value.
+ */
+uint64_t addln_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Test and benchmark only.  Caps the grid of the persistent CTA-per-row
+ * kernels at `ctas` CTAs (0 = one wave of resident CTAs, the default).
+ * Returns the previous cap.
+ */
+int64_t addln_set_grid_cap(int64_t ctas);
+
+/* Name of the kernel path the last add_layernorm_fwd / layernorm_fwd call on
+ * this host thread launched (static text; "none" before the first launch). */
+const char *addln_last_path(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADDLN_H */

@@ -1,0 +1,23 @@
+"""GB300 (sm_103a) fused residual-Add + LayerNorm.
+
+The compute lives in ``_build/libaddln.so`` (hand-written CUDA kernels behind
+the C ABI of ``include/addln.h``); ``binding`` marshals PyTorch tensors to it.
+"""
+from .binding import (  # noqa: F401
+    AddLNError,
+    add_layernorm_fwd,
+    add_fwd,
+    layernorm_fwd,
+    add_layernorm,
+    add_then_layernorm,
+    addln_get_device_error,
+    addln_set_force_path,
+    addln_set_wait_limit_ns,
+    addln_set_grid_cap,
+    addln_last_path,
+    addln_max_hidden,
+    addln_strerror,
+    lib,
+    FP32, FP16, BF16,
+    PATH_AUTO, PATH_WARP_VEC, PATH_CTA_TMA, PATH_CTA_VEC, PATH_SCALAR,
+)

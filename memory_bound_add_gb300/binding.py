@@ -1,0 +1,239 @@
+"""Thin ctypes binding over the C ABI in include/addln.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libaddln.so``.  Tensors are PyTorch CUDA tensors (PyTorch
+supplies device memory and the current stream); raw integer device pointers
+are accepted too.  There is no CPU fallback: if the library is missing this
+module raises on import of the first function call.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libaddln.so")
+
+FP32, FP16, BF16 = 0, 1, 2
+DTYPE_CODE = {torch.float32: FP32, torch.float16: FP16, torch.bfloat16: BF16}
+
+OK = 0
+ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_EPS, ERR_ALIAS = -1, -2, -3, -4, -5
+ERR_LAUNCH, ERR_UNSUPPORTED, ERR_DEVICE_TIMEOUT, ERR_CUDA = -6, -7, -8, -9
+
+PATH_AUTO, PATH_WARP_VEC, PATH_CTA_TMA, PATH_CTA_VEC, PATH_SCALAR = 0, 1, 2, 3, 4
+
+# Every symbol include/addln.h declares, with its ctypes signature.
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+SIGNATURES = {
+    "add_layernorm_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                                         ctypes.c_float, ctypes.c_int, _P]),
+    "add_fwd": (ctypes.c_int, [_P, _P, _P, _I64, ctypes.c_int, _P]),
+    "layernorm_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_float,
+                                     ctypes.c_int, _P]),
+    "addln_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "addln_max_hidden": (ctypes.c_int64, [ctypes.c_int]),
+    "addln_get_device_error": (ctypes.c_int, [_P]),
+    "addln_set_force_path": (ctypes.c_int, [ctypes.c_int]),
+    "addln_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+    "addln_set_grid_cap": (ctypes.c_int64, [ctypes.c_int64]),
+    "addln_last_path": (ctypes.c_char_p, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class AddLNError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (code {code})")
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it first "
+                        "(python -c 'import __graft_entry__ as g; g.build()')")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in SIGNATURES.items():
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().addln_strerror(int(code)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != OK:
+        raise AddLNError(rc, where)
+
+
+def _rows_shape(x):
+    if x.dim() < 1:
+        raise ValueError("x must have at least one dimension (the hidden dim)")
+    H = x.shape[-1]
+    rows = x.numel() // H if H else 0
+    return rows, H
+
+
+def _require(t, name, dtype=None, like=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if like is not None and t.numel() != like.numel():
+        raise ValueError(f"{name} has {t.numel()} elements, expected {like.numel()}")
+
+
+def add_layernorm_fwd(x, r, gamma, beta, y, resid_out=None, mean=None, rstd=None,
+                      eps: float = 1e-5, stream=None, rows=None, H=None, dtype=None):
+    """Fused residual-Add + LayerNorm into caller-provided outputs.
+
+    With tensors, rows and H come from x's shape ([..., H]) and dtype from
+    x.dtype.  With raw device pointers, pass rows, H and dtype explicitly.
+    """
+    if isinstance(x, torch.Tensor):
+        rows_, H_ = _rows_shape(x)
+        dtype_ = DTYPE_CODE.get(x.dtype)
+        if dtype_ is None:
+            raise ValueError(f"unsupported dtype {x.dtype}")
+        for t, n in ((x, "x"), (r, "r"), (y, "y"), (resid_out, "resid_out")):
+            if t is not None and isinstance(t, torch.Tensor):
+                _require(t, n, x.dtype, like=x)
+        for t, n in ((gamma, "gamma"), (beta, "beta")):
+            if isinstance(t, torch.Tensor):
+                _require(t, n, torch.float32)
+                if t.numel() != H_:
+                    raise ValueError(f"{n} must have H={H_} elements")
+        for t, n in ((mean, "mean"), (rstd, "rstd")):
+            if isinstance(t, torch.Tensor):
+                _require(t, n, torch.float32)
+                if t.numel() != rows_:
+                    raise ValueError(f"{n} must have rows={rows_} elements")
+        rows = rows_ if rows is None else rows
+        H = H_ if H is None else H
+        dtype = dtype_ if dtype is None else dtype
+    rc = lib().add_layernorm_fwd(_ptr(x), _ptr(r), _ptr(gamma), _ptr(beta), _ptr(y),
+                                 _ptr(resid_out), _ptr(mean), _ptr(rstd), int(rows), int(H),
+                                 float(eps), int(dtype), _stream(stream))
+    _check(rc, "add_layernorm_fwd")
+
+
+def layernorm_fwd(a, gamma, beta, y, mean=None, rstd=None, eps: float = 1e-5, stream=None,
+                  rows=None, H=None, dtype=None):
+    """LayerNorm of a stored [rows, H] tensor (second kernel of the unfused chain)."""
+    if isinstance(a, torch.Tensor):
+        rows_, H_ = _rows_shape(a)
+        _require(a, "a")
+        _require(y, "y", a.dtype, like=a)
+        rows = rows_ if rows is None else rows
+        H = H_ if H is None else H
+        dtype = DTYPE_CODE[a.dtype] if dtype is None else dtype
+    rc = lib().layernorm_fwd(_ptr(a), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean), _ptr(rstd),
+                             int(rows), int(H), float(eps), int(dtype), _stream(stream))
+    _check(rc, "layernorm_fwd")
+
+
+def add_fwd(x, r, a, stream=None, n=None, dtype=None):
+    """A = X + R elementwise (first kernel of the unfused chain)."""
+    if isinstance(x, torch.Tensor):
+        _require(x, "x")
+        _require(r, "r", x.dtype, like=x)
+        _require(a, "a", x.dtype, like=x)
+        n = x.numel() if n is None else n
+        dtype = DTYPE_CODE[x.dtype] if dtype is None else dtype
+    _check(lib().add_fwd(_ptr(x), _ptr(r), _ptr(a), int(n), int(dtype), _stream(stream)), "add_fwd")
+
+
+def addln_max_hidden(dtype: int) -> int:
+    return int(lib().addln_max_hidden(int(dtype)))
+
+
+def addln_get_device_error(stream=None) -> int:
+    return int(lib().addln_get_device_error(_stream(stream)))
+
+
+def addln_set_force_path(path: int) -> int:
+    return int(lib().addln_set_force_path(int(path)))
+
+
+def addln_set_wait_limit_ns(ns: int) -> int:
+    return int(lib().addln_set_wait_limit_ns(int(ns)))
+
+
+def addln_set_grid_cap(ctas: int) -> int:
+    return int(lib().addln_set_grid_cap(int(ctas)))
+
+
+def addln_last_path() -> str:
+    return lib().addln_last_path().decode()
+
+
+def addln_strerror(code: int) -> str:
+    return strerror(code)
+
+
+# --------------------------------------------------------------- convenience
+def add_layernorm(x, r, gamma, beta, eps: float = 1e-5, want_resid: bool = False,
+                  want_stats: bool = False, stream=None):
+    """Allocate outputs with PyTorch and run add_layernorm_fwd.
+
+    Returns (y, resid_out or None, mean or None, rstd or None).
+    """
+    y = torch.empty_like(x)
+    a = torch.empty_like(x) if want_resid else None
+    rows, _ = _rows_shape(x)
+    mean = torch.empty(rows, dtype=torch.float32, device=x.device) if want_stats else None
+    rstd = torch.empty(rows, dtype=torch.float32, device=x.device) if want_stats else None
+    add_layernorm_fwd(x, r, gamma, beta, y, a, mean, rstd, eps=eps, stream=stream)
+    return y, a, mean, rstd
+
+
+def add_then_layernorm(x, r, gamma, beta, eps: float = 1e-5, want_stats: bool = False,
+                       stream=None):
+    """The unfused two-kernel chain: A = X + R to memory, then LayerNorm(A).
+
+    Returns (y, a, mean or None, rstd or None).
+    """
+    a = torch.empty_like(x)
+    y = torch.empty_like(x)
+    rows, _ = _rows_shape(x)
+    mean = torch.empty(rows, dtype=torch.float32, device=x.device) if want_stats else None
+    rstd = torch.empty(rows, dtype=torch.float32, device=x.device) if want_stats else None
+    add_fwd(x, r, a, stream=stream)
+    layernorm_fwd(a, gamma, beta, y, mean, rstd, eps=eps, stream=stream)
+    return y, a, mean, rstd

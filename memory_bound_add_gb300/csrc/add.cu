@@ -1,0 +1,92 @@
+// Unfused baseline, step 1: the separate residual-add kernel of
+// "算子融合的收益量化" section 1 -- read X and R, write A = X + R in the I/O
+// dtype (rounded to nearest-even from the fp32 sum).  Grid-stride over
+// 16-byte vectors with four independent vectors per thread per step; the
+// last n % VEC elements (and misaligned buffers) take element accesses.
+#include "../../include/addln.h"
+#include "common.cuh"
+
+namespace addln {
+
+constexpr int kAddThreads = 256;
+constexpr int kAddUnroll = 4;
+
+template <int DT>
+__global__ void __launch_bounds__(kAddThreads) k_add_vec(const void* x, const void* r, void* a,
+                                                         int64_t nvec, int64_t n) {
+  using IO = Io<DT>;
+  constexpr int VEC = IO::kVec;
+  const uint4* xv = static_cast<const uint4*>(x);
+  const uint4* rv = static_cast<const uint4*>(r);
+  uint4* av = static_cast<uint4*>(a);
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kAddThreads * kAddUnroll;
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kAddThreads * kAddUnroll + threadIdx.x;
+       i0 < nvec; i0 += step) {
+    uint4 xs[kAddUnroll], rs[kAddUnroll];
+#pragma unroll
+    for (int u = 0; u < kAddUnroll; ++u) {
+      const int64_t i = i0 + static_cast<int64_t>(u) * kAddThreads;
+      if (i < nvec) {
+        xs[u] = ld_stream_v4(xv + i);
+        rs[u] = ld_stream_v4(rv + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kAddUnroll; ++u) {
+      const int64_t i = i0 + static_cast<int64_t>(u) * kAddThreads;
+      if (i < nvec) {
+        float f[VEC], g[VEC];
+        IO::unpack(xs[u], f);
+        IO::unpack(rs[u], g);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f[e] += g[e];
+        st_stream_v4(av + i, IO::pack(f));
+      }
+    }
+  }
+  // tail elements past the last whole vector
+  if (blockIdx.x == 0) {
+    for (int64_t j = nvec * VEC + threadIdx.x; j < n; j += kAddThreads)
+      IO::store1(a, j, IO::load1(x, j) + IO::load1(r, j));
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kAddThreads) k_add_scalar(const void* x, const void* r, void* a,
+                                                            int64_t n) {
+  using IO = Io<DT>;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kAddThreads;
+  for (int64_t j = static_cast<int64_t>(blockIdx.x) * kAddThreads + threadIdx.x; j < n; j += step)
+    IO::store1(a, j, IO::load1(x, j) + IO::load1(r, j));
+}
+
+template <int DT>
+static int launch_add_t(const void* x, const void* r, void* a, int64_t n, const LaunchCtx& c) {
+  constexpr int VEC = Io<DT>::kVec;
+  const int64_t max_blocks = static_cast<int64_t>(c.dev.sms) * (2048 / kAddThreads);
+  auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  cudaStream_t s = static_cast<cudaStream_t>(c.stream);
+  if (al(x) && al(r) && al(a)) {
+    const int64_t nvec = n / VEC;
+    int64_t blocks = (nvec + kAddThreads * kAddUnroll - 1) / (kAddThreads * kAddUnroll);
+    if (blocks > max_blocks) blocks = max_blocks;
+    if (blocks < 1) blocks = 1;
+    k_add_vec<DT><<<static_cast<unsigned>(blocks), kAddThreads, 0, s>>>(x, r, a, nvec, n);
+  } else {
+    int64_t blocks = (n + kAddThreads - 1) / kAddThreads;
+    if (blocks > max_blocks) blocks = max_blocks;
+    k_add_scalar<DT><<<static_cast<unsigned>(blocks), kAddThreads, 0, s>>>(x, r, a, n);
+  }
+  return cudaGetLastError() == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+}
+
+int launch_add(int dtype, const void* x, const void* r, void* a, int64_t n, const LaunchCtx& c) {
+  switch (dtype) {
+    case kF32: return launch_add_t<kF32>(x, r, a, n, c);
+    case kF16: return launch_add_t<kF16>(x, r, a, n, c);
+    case kBF16: return launch_add_t<kBF16>(x, r, a, n, c);
+    default: return ADDLN_ERR_DTYPE;
+  }
+}
+
+}  // namespace addln

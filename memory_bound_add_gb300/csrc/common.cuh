@@ -1,0 +1,288 @@
+// Device-side building blocks shared by the row kernels: I/O dtype traits,
+// 16-byte vector (un)packing, inline-PTX memory operations (streaming loads
+// and stores, mbarrier, TMA bulk copy) and the Chan combination of partial
+// (count, mean, M2) statistics.
+//
+// The statistics follow the LayerNorm of "算子融合与Kernel合并" 4.2 (mean,
+// then the biased variance around it, eps inside the square root) but are
+// gathered in one pass over registers: each thread takes the exact two-pass
+// mean/M2 of the values it holds, and partial results are merged with Chan,
+// Golub and LeVeque's pairwise update.  The page's own one-pass shortcut
+// (sum and sum of squares, same page 4.3) is avoided: it cancels when the
+// row mean is large against its spread.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "launch.h"
+
+namespace addln {
+
+// ------------------------------------------------------------ dtype traits
+template <int DT>
+struct Io;
+
+template <>
+struct Io<kF32> {
+  static constexpr int kBytes = 4;
+  static constexpr int kVec = 4;  // elements per 16-byte vector
+  __device__ static __forceinline__ void unpack(const uint4& u, float* f) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+  __device__ static __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+  __device__ static __forceinline__ float load1(const void* p, int64_t i) {
+    return __ldg(static_cast<const float*>(p) + i);
+  }
+  __device__ static __forceinline__ void store1(void* p, int64_t i, float v) {
+    static_cast<float*>(p)[i] = v;
+  }
+};
+
+template <>
+struct Io<kF16> {
+  static constexpr int kBytes = 2;
+  static constexpr int kVec = 8;
+  __device__ static __forceinline__ float2 w2f(uint32_t w) {
+    __half2 h = *reinterpret_cast<__half2*>(&w);
+    return __half22float2(h);
+  }
+  __device__ static __forceinline__ uint32_t f2w(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static __forceinline__ void unpack(const uint4& u, float* f) {
+    float2 t;
+    t = w2f(u.x); f[0] = t.x; f[1] = t.y;
+    t = w2f(u.y); f[2] = t.x; f[3] = t.y;
+    t = w2f(u.z); f[4] = t.x; f[5] = t.y;
+    t = w2f(u.w); f[6] = t.x; f[7] = t.y;
+  }
+  __device__ static __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(f2w(f[0], f[1]), f2w(f[2], f[3]), f2w(f[4], f[5]), f2w(f[6], f[7]));
+  }
+  __device__ static __forceinline__ float load1(const void* p, int64_t i) {
+    unsigned short b = __ldg(static_cast<const unsigned short*>(p) + i);
+    return __half2float(__ushort_as_half(b));
+  }
+  __device__ static __forceinline__ void store1(void* p, int64_t i, float v) {
+    static_cast<__half*>(p)[i] = __float2half_rn(v);
+  }
+};
+
+template <>
+struct Io<kBF16> {
+  static constexpr int kBytes = 2;
+  static constexpr int kVec = 8;
+  __device__ static __forceinline__ float2 w2f(uint32_t w) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
+    return __bfloat1622float2(h);
+  }
+  __device__ static __forceinline__ uint32_t f2w(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static __forceinline__ void unpack(const uint4& u, float* f) {
+    float2 t;
+    t = w2f(u.x); f[0] = t.x; f[1] = t.y;
+    t = w2f(u.y); f[2] = t.x; f[3] = t.y;
+    t = w2f(u.z); f[4] = t.x; f[5] = t.y;
+    t = w2f(u.w); f[6] = t.x; f[7] = t.y;
+  }
+  __device__ static __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(f2w(f[0], f[1]), f2w(f[2], f[3]), f2w(f[4], f[5]), f2w(f[6], f[7]));
+  }
+  __device__ static __forceinline__ float load1(const void* p, int64_t i) {
+    unsigned short b = __ldg(static_cast<const unsigned short*>(p) + i);
+    return __bfloat162float(__ushort_as_bfloat16(b));
+  }
+  __device__ static __forceinline__ void store1(void* p, int64_t i, float v) {
+    static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+  }
+};
+
+// --------------------------------------------------------- global memory
+// Streaming 16-byte load of data that is read exactly once: read-only path,
+// no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// Streaming 16-byte store (evict-first): outputs are not re-read here.
+__device__ __forceinline__ void st_stream_v4(void* p, const uint4& v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// gamma / beta: re-read by every row, so keep them cached.
+__device__ __forceinline__ float4 ld_param_f4(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+// ---------------------------------------------------------- shared memory
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// --------------------------------------------------- mbarrier + TMA bulk
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// One-dimensional bulk copy global -> shared, completing `bytes` of the
+// barrier's transaction count.  src, dst 16-byte aligned; bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// L2 policy for data read exactly once.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for phase `parity` of the barrier, giving up after limit_ns
+// nanoseconds (limit 0: give up without waiting).  Returns true once the
+// phase has completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+  if (limit_ns == 0) return false;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// ------------------------------------------------------------- statistics
+struct Stats {
+  float n;   // element count (exact in fp32 up to 2^24)
+  float m;   // mean
+  float M2;  // sum of squared deviations from m
+};
+
+// Chan et al. pairwise update.  Not symmetric in rounding, so callers always
+// pass the lower-indexed partial as `a`; every thread then holds bitwise the
+// same totals.  An empty side (n = 0) leaves the other side unchanged.
+__device__ __forceinline__ Stats chan_combine(const Stats& a, const Stats& b) {
+  Stats o;
+  o.n = a.n + b.n;
+  const float wb = __fdiv_rn(b.n, fmaxf(o.n, 1.0f));
+  const float d = b.m - a.m;
+  o.m = fmaf(d, wb, a.m);
+  o.M2 = fmaf(d * d * a.n, wb, a.M2 + b.M2);
+  return o;
+}
+
+// Butterfly all-reduce over the 32 lanes with a fixed lower/upper order at
+// every level, so all lanes finish with identical (n, m, M2).
+__device__ __forceinline__ Stats warp_allreduce(Stats s, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    Stats o;
+    o.n = __shfl_xor_sync(0xffffffffu, s.n, off);
+    o.m = __shfl_xor_sync(0xffffffffu, s.m, off);
+    o.M2 = __shfl_xor_sync(0xffffffffu, s.M2, off);
+    const bool upper = (lane & off) != 0;
+    const Stats lo = upper ? o : s;
+    const Stats hi = upper ? s : o;
+    s = chan_combine(lo, hi);
+  }
+  return s;
+}
+
+// Two-pass statistics of the values one thread holds: exact mean of its own
+// values (IEEE division, so a constant run gives its value back exactly),
+// then the sum of squared deviations around it.
+template <int NV, int VEC>
+__device__ __forceinline__ Stats thread_stats(const float (&v)[NV][VEC], const bool (&ok)[NV]) {
+  float sum = 0.f;
+  int cnt = 0;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    if (ok[k]) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) sum += v[k][e];
+      cnt += VEC;
+    }
+  }
+  Stats s;
+  s.n = static_cast<float>(cnt);
+  s.m = cnt ? __fdiv_rn(sum, s.n) : 0.f;
+  float M2 = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    if (ok[k]) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const float d = v[k][e] - s.m;
+        M2 = fmaf(d, d, M2);
+      }
+    }
+  }
+  s.M2 = M2;
+  return s;
+}
+
+// rstd = 1 / sqrt(M2 / H + eps), from the row totals.
+__device__ __forceinline__ float row_rstd(const Stats& t, int H, float eps) {
+  const float var = __fdiv_rn(t.M2, static_cast<float>(H));
+  return rsqrtf(var + eps);
+}
+
+}  // namespace addln

@@ -1,0 +1,69 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Host-only types; no CUDA headers needed to include it.
+#pragma once
+
+#include <stdint.h>
+
+namespace addln {
+
+enum Dtype : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+// Arguments of one row-kernel launch.  x, r, y, a are [rows, H] in the I/O
+// dtype; r == nullptr means LayerNorm of x alone; a, mean, rstd optional.
+struct RowArgs {
+  const void* x;
+  const void* r;
+  const float* gamma;
+  const float* beta;
+  void* y;
+  void* a;
+  float* mean;
+  float* rstd;
+  int64_t rows;
+  int H;
+  float eps;
+  uint64_t wait_limit_ns;  // bound on mbarrier waits (TMA path)
+};
+
+// Per-device facts the dispatcher sizes grids and shared memory with.
+struct DeviceInfo {
+  int device;
+  int sms;
+  int smem_optin;  // max dynamic shared memory per block (opt-in)
+  int l2_bytes;
+};
+
+struct LaunchCtx {
+  void* stream;  // cudaStream_t
+  DeviceInfo dev;
+  int64_t grid_cap;  // 0 = one wave of resident CTAs
+};
+
+// Each launcher returns 0, or ADDLN_ERR_UNSUPPORTED when its kernel family
+// cannot run these arguments, or ADDLN_ERR_LAUNCH.  `path_name` receives the
+// static name of the launched kernel.
+
+// One warp per row (H <= 1024).  vec: 16-byte vector loads (requires every
+// row pointer and gamma/beta 16-byte aligned and H a multiple of the vector).
+int launch_warp_row(int dtype, bool vec, const RowArgs& p, const LaunchCtx& c,
+                    const char** path_name);
+
+// One CTA per row, persistent over rows.  tma: rows staged into shared
+// memory by bulk copies; otherwise 16-byte vector loads to registers.
+int launch_cta_row(int dtype, bool tma, const RowArgs& p, const LaunchCtx& c,
+                   const char** path_name);
+
+// One CTA per row, element-wise loads, any alignment, H <= max.
+int launch_cta_scalar(int dtype, const RowArgs& p, const LaunchCtx& c, const char** path_name);
+
+// A = X + R over n elements.
+int launch_add(int dtype, const void* x, const void* r, void* a, int64_t n, const LaunchCtx& c);
+
+// Device error word (set by a kernel whose bounded wait ran out).
+int read_and_clear_device_error(void* stream, int* code);
+
+// Largest H per dtype (shared memory and register budget of the CTA paths).
+constexpr int64_t kMaxHidden16 = 32768;
+constexpr int64_t kMaxHidden32 = 16384;
+
+}  // namespace addln

@@ -1,0 +1,401 @@
+// One CTA per row: fused residual add + LayerNorm for long rows (H > 1024).
+//
+// The grid is persistent (one wave of resident CTAs, sized from the SM count
+// and the occupancy the kernel reaches); CTA b takes rows b, b + grid, ...
+//
+// TMA variant: thread 0 stages whole rows of X and R into shared memory with
+// one-dimensional bulk copies (cp.async.bulk, completion counted on an
+// mbarrier).  With two stages the copy of the CTA's next-but-one row is in
+// flight while the current row is reduced and normalised, so every SM keeps
+// row-sized requests outstanding against HBM.  Each thread moves its slice
+// from shared memory into registers once; the reduction and the normalisation
+// both run on those registers, and Y / A go straight to global memory with
+// 16-byte streaming stores.
+//
+// Vector variant: the same kernel with 16-byte loads from global memory in
+// place of the staging copies (kept for comparison and for forced runs).
+//
+// Scalar variant: element loads for rows whose bytes or base addresses are
+// not 16-byte aligned; the fp32 row sum is kept in shared memory.
+//
+// Waits on the staging copies are bounded.  A wait that runs out sets the
+// device error word, waits (bounded again) for the CTA's copies still in
+// flight so no copy lands in reused shared memory, and the CTA returns.
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/addln.h"
+#include "common.cuh"
+
+namespace addln {
+
+__device__ int g_device_error = 0;
+
+constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s
+
+template <int DT, int THREADS, int NV, bool TMA>
+__global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int stages) {
+  using IO = Io<DT>;
+  constexpr int VEC = IO::kVec;
+  constexpr int S = IO::kBytes;
+  constexpr int NW = THREADS / 32;
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H = p.H;
+  const int nvec = H / VEC;
+  const bool has_r = p.r != nullptr;
+  const uint32_t row_bytes = static_cast<uint32_t>(H) * S;  // multiple of 16
+  const uint32_t rb = (row_bytes + 127u) & ~127u;
+  const uint32_t slot = has_r ? 2u * rb : rb;
+  const uint32_t data_bytes = TMA ? static_cast<uint32_t>(stages) * slot : 0u;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + data_bytes);
+  Stats* red = reinterpret_cast<Stats*>(smem + data_bytes + 16);  // [2][NW]
+  const uint32_t smem0 = smem_addr(smem);
+
+  bool ok[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) ok[k] = (tid + THREADS * k) < nvec;
+
+  const int64_t stride = gridDim.x;
+  int64_t row = blockIdx.x;
+  uint64_t policy = 0;
+
+  if constexpr (TMA) {
+    if (tid == 0) {
+      for (int s = 0; s < stages; ++s) mbar_init(smem_addr(&bars[s]), 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    policy = policy_evict_first();
+  }
+
+  // Thread 0: stage row `rr` of X (and R) into stage `s`.
+  auto issue = [&](int s, int64_t rr) {
+    const uint32_t bar = smem_addr(&bars[s]);
+    mbar_arrive_expect_tx(bar, has_r ? 2u * row_bytes : row_bytes);
+    const int64_t off = rr * static_cast<int64_t>(row_bytes);
+    bulk_g2s(smem0 + s * slot, static_cast<const char*>(p.x) + off, row_bytes, bar, policy);
+    if (has_r)
+      bulk_g2s(smem0 + s * slot + rb, static_cast<const char*>(p.r) + off, row_bytes, bar, policy);
+  };
+
+  if constexpr (TMA) {
+    if (tid == 0)
+      for (int s = 0; s < stages; ++s)
+        if (row + s * stride < p.rows) issue(s, row + s * stride);
+  }
+
+  for (int64_t it = 0; row < p.rows; ++it, row += stride) {
+    const int64_t base = row * static_cast<int64_t>(H);
+    float v[NV][VEC];
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
+
+    bool timed_out = false;
+    if constexpr (TMA) {
+      const int s = static_cast<int>(it % stages);
+      const uint32_t parity = static_cast<uint32_t>((it / stages) & 1);
+      timed_out = !mbar_wait_bounded(smem_addr(&bars[s]), parity, p.wait_limit_ns);
+      const uint32_t xs = smem0 + s * slot;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (ok[k]) IO::unpack(ld_shared_v4(xs + (tid + THREADS * k) * 16), v[k]);
+      if (has_r) {
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+          if (ok[k]) {
+            float t[VEC];
+            IO::unpack(ld_shared_v4(xs + rb + (tid + THREADS * k) * 16), t);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[k][e] += t[e];
+          }
+        }
+      }
+    } else {
+      const char* xrow = static_cast<const char*>(p.x) + base * S;
+      uint4 xv[NV], rv[NV];
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (ok[k]) xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(tid + THREADS * k) * 16);
+      if (has_r) {
+        const char* rrow = static_cast<const char*>(p.r) + base * S;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          if (ok[k]) rv[k] = ld_stream_v4(rrow + static_cast<int64_t>(tid + THREADS * k) * 16);
+      }
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        if (ok[k]) {
+          IO::unpack(xv[k], v[k]);
+          if (has_r) {
+            float t[VEC];
+            IO::unpack(rv[k], t);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[k][e] += t[e];
+          }
+        }
+      }
+    }
+
+    // ---- statistics: per-thread two-pass, warp butterfly, CTA merge
+    Stats st = thread_stats<NV, VEC>(v, ok);
+    st = warp_allreduce(st, lane);
+    Stats* rbuf = red + (it & 1) * NW;
+    if (lane == 0) rbuf[warp] = st;
+
+    if constexpr (TMA) {
+      // Also the point after which no thread reads stage s any more.
+      if (__syncthreads_or(timed_out)) {
+        if (tid == 0) {
+          atomicExch(&g_device_error, ADDLN_ERR_DEVICE_TIMEOUT);
+          for (int j = 0; j < stages; ++j) {
+            const int64_t itj = it + j;
+            if (row + j * stride < p.rows)
+              mbar_wait_bounded(smem_addr(&bars[itj % stages]),
+                                static_cast<uint32_t>((itj / stages) & 1), kDrainLimitNs);
+          }
+        }
+        return;
+      }
+      if (tid == 0) {
+        const int64_t next = row + stages * stride;
+        if (next < p.rows) issue(static_cast<int>(it % stages), next);
+      }
+    } else {
+      __syncthreads();
+    }
+
+    Stats tot = {0.f, 0.f, 0.f};
+    if (lane < NW) tot = rbuf[lane];
+    tot = warp_allreduce(tot, lane);
+    const float mean = tot.m;
+    const float rstd = row_rstd(tot, H, p.eps);
+
+    // ---- normalise + affine from registers, store
+    char* yrow = static_cast<char*>(p.y) + base * S;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (ok[k]) {
+        const int c = tid + THREADS * k;
+        float o[VEC];
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+          const float4 g = ld_param_f4(p.gamma + c * VEC + 4 * q);
+          const float4 b = ld_param_f4(p.beta + c * VEC + 4 * q);
+          o[4 * q + 0] = fmaf((v[k][4 * q + 0] - mean) * rstd, g.x, b.x);
+          o[4 * q + 1] = fmaf((v[k][4 * q + 1] - mean) * rstd, g.y, b.y);
+          o[4 * q + 2] = fmaf((v[k][4 * q + 2] - mean) * rstd, g.z, b.z);
+          o[4 * q + 3] = fmaf((v[k][4 * q + 3] - mean) * rstd, g.w, b.w);
+        }
+        st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::pack(o));
+      }
+    }
+    if (p.a != nullptr) {
+      char* arow = static_cast<char*>(p.a) + base * S;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (ok[k]) st_stream_v4(arow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::pack(v[k]));
+    }
+    if (tid == 0) {
+      if (p.mean != nullptr) p.mean[row] = mean;
+      if (p.rstd != nullptr) p.rstd[row] = rstd;
+    }
+  }
+}
+
+// Element-wise variant: any alignment, any H up to the maximum.  Each thread
+// keeps the fp32 sums of its own elements (j = tid + THREADS*k) in shared
+// memory, so no thread reads another's slots and only the statistics need a
+// barrier.
+template <int DT, int THREADS>
+__global__ void __launch_bounds__(THREADS) k_cta_scalar(const RowArgs p) {
+  using IO = Io<DT>;
+  constexpr int NW = THREADS / 32;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int H = p.H;
+  float* sa = reinterpret_cast<float*>(smem);
+  Stats* red = reinterpret_cast<Stats*>(smem + ((static_cast<uint32_t>(H) * 4u + 127u) & ~127u));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool has_r = p.r != nullptr;
+
+  int64_t it = 0;
+  for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
+    const int64_t base = row * static_cast<int64_t>(H);
+    float sum = 0.f;
+    int cnt = 0;
+#pragma unroll 8
+    for (int j = tid; j < H; j += THREADS) {
+      float a = IO::load1(p.x, base + j);
+      if (has_r) a += IO::load1(p.r, base + j);
+      sa[j] = a;
+      sum += a;
+      ++cnt;
+    }
+    Stats st;
+    st.n = static_cast<float>(cnt);
+    st.m = cnt ? __fdiv_rn(sum, st.n) : 0.f;
+    float M2 = 0.f;
+    for (int j = tid; j < H; j += THREADS) {
+      const float d = sa[j] - st.m;
+      M2 = fmaf(d, d, M2);
+    }
+    st.M2 = M2;
+    st = warp_allreduce(st, lane);
+    Stats* rbuf = red + (it & 1) * NW;
+    if (lane == 0) rbuf[warp] = st;
+    __syncthreads();
+    Stats tot = {0.f, 0.f, 0.f};
+    if (lane < NW) tot = rbuf[lane];
+    tot = warp_allreduce(tot, lane);
+    const float mean = tot.m;
+    const float rstd = row_rstd(tot, H, p.eps);
+#pragma unroll 4
+    for (int j = tid; j < H; j += THREADS) {
+      const float a = sa[j];
+      IO::store1(p.y, base + j, fmaf((a - mean) * rstd, __ldg(p.gamma + j), __ldg(p.beta + j)));
+      if (p.a != nullptr) IO::store1(p.a, base + j, a);
+    }
+    if (tid == 0) {
+      if (p.mean != nullptr) p.mean[row] = mean;
+      if (p.rstd != nullptr) p.rstd[row] = rstd;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host
+namespace {
+
+struct FuncKey {
+  const void* f;
+  int device;
+  int smem;
+  bool operator==(const FuncKey& o) const { return f == o.f && device == o.device && smem == o.smem; }
+};
+struct FuncKeyHash {
+  size_t operator()(const FuncKey& k) const {
+    return std::hash<const void*>()(k.f) ^ (static_cast<size_t>(k.device) << 20) ^
+           (static_cast<size_t>(k.smem) << 28);
+  }
+};
+
+std::mutex g_occ_mu;
+std::unordered_map<FuncKey, int, FuncKeyHash> g_occ;  // resident CTAs per SM
+
+// Resident CTAs per SM for (kernel, dynamic smem) on this device; raises the
+// kernel's dynamic shared memory limit first when needed.  -1 on error.
+int resident_ctas(const void* f, int threads, int smem, const DeviceInfo& dev) {
+  const FuncKey key{f, dev.device, smem};
+  {
+    std::lock_guard<std::mutex> g(g_occ_mu);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+  }
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return -1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, threads, smem) != cudaSuccess) return -1;
+  std::lock_guard<std::mutex> g(g_occ_mu);
+  g_occ[key] = n;
+  return n;
+}
+
+int64_t persistent_grid(int64_t rows, int per_sm, const LaunchCtx& c) {
+  int64_t g = static_cast<int64_t>(per_sm) * c.dev.sms;
+  if (c.grid_cap > 0 && c.grid_cap < g) g = c.grid_cap;
+  if (rows < g) g = rows;
+  return g;
+}
+
+template <int DT, int THREADS, int NV, bool TMA>
+int launch_row(const RowArgs& p, const LaunchCtx& c) {
+  constexpr int S = Io<DT>::kBytes;
+  const uint32_t row_bytes = static_cast<uint32_t>(p.H) * S;
+  const uint32_t rb = (row_bytes + 127u) & ~127u;
+  const uint32_t slot = p.r ? 2u * rb : rb;
+  const uint32_t extra = 16u + 2u * (THREADS / 32) * sizeof(Stats);
+  int stages = 0;
+  uint32_t smem = extra;
+  if (TMA) {
+    stages = (2u * slot + extra <= static_cast<uint32_t>(c.dev.smem_optin) / 2u) ? 2 : 1;
+    smem = stages * slot + extra;
+    if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
+  }
+  const void* f = reinterpret_cast<const void*>(&k_cta_row<DT, THREADS, NV, TMA>);
+  const int per_sm = resident_ctas(f, THREADS, static_cast<int>(smem), c.dev);
+  if (per_sm < 0) return ADDLN_ERR_CUDA;
+  if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
+  const int64_t grid = persistent_grid(p.rows, per_sm, c);
+  k_cta_row<DT, THREADS, NV, TMA>
+      <<<static_cast<unsigned>(grid), THREADS, smem, static_cast<cudaStream_t>(c.stream)>>>(p, stages);
+  return cudaGetLastError() == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+}
+
+// (threads, vectors per thread) by the number of 16-byte vectors in a row.
+template <int DT, bool TMA>
+int launch_row_dispatch(const RowArgs& p, const LaunchCtx& c, const char** name) {
+  constexpr int VEC = Io<DT>::kVec;
+  const int nvec = p.H / VEC;
+  if (nvec <= 128 * 2) { *name = TMA ? "cta_tma_t128_nv2" : "cta_vec_t128_nv2"; return launch_row<DT, 128, 2, TMA>(p, c); }
+  if (nvec <= 128 * 4) { *name = TMA ? "cta_tma_t128_nv4" : "cta_vec_t128_nv4"; return launch_row<DT, 128, 4, TMA>(p, c); }
+  if (nvec <= 256 * 4) { *name = TMA ? "cta_tma_t256_nv4" : "cta_vec_t256_nv4"; return launch_row<DT, 256, 4, TMA>(p, c); }
+  if (nvec <= 512 * 4) { *name = TMA ? "cta_tma_t512_nv4" : "cta_vec_t512_nv4"; return launch_row<DT, 512, 4, TMA>(p, c); }
+  // 1024 threads cap registers at 64 a thread: only the shared-memory staged
+  // variant fits there without spilling.
+  if constexpr (TMA) {
+    if (nvec <= 1024 * 4) { *name = "cta_tma_t1024_nv4"; return launch_row<DT, 1024, 4, true>(p, c); }
+  }
+  return ADDLN_ERR_UNSUPPORTED;
+}
+
+template <int DT>
+int launch_scalar_impl(const RowArgs& p, const LaunchCtx& c) {
+  constexpr int THREADS = 512;
+  const uint32_t smem = ((static_cast<uint32_t>(p.H) * 4u + 127u) & ~127u) +
+                        2u * (THREADS / 32) * sizeof(Stats);
+  if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
+  const void* f = reinterpret_cast<const void*>(&k_cta_scalar<DT, THREADS>);
+  const int per_sm = resident_ctas(f, THREADS, static_cast<int>(smem), c.dev);
+  if (per_sm < 0) return ADDLN_ERR_CUDA;
+  if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
+  const int64_t grid = persistent_grid(p.rows, per_sm, c);
+  k_cta_scalar<DT, THREADS>
+      <<<static_cast<unsigned>(grid), THREADS, smem, static_cast<cudaStream_t>(c.stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+int launch_cta_row(int dtype, bool tma, const RowArgs& p, const LaunchCtx& c, const char** name) {
+  switch (dtype) {
+    case kF32: return tma ? launch_row_dispatch<kF32, true>(p, c, name) : launch_row_dispatch<kF32, false>(p, c, name);
+    case kF16: return tma ? launch_row_dispatch<kF16, true>(p, c, name) : launch_row_dispatch<kF16, false>(p, c, name);
+    case kBF16: return tma ? launch_row_dispatch<kBF16, true>(p, c, name) : launch_row_dispatch<kBF16, false>(p, c, name);
+    default: return ADDLN_ERR_DTYPE;
+  }
+}
+
+int launch_cta_scalar(int dtype, const RowArgs& p, const LaunchCtx& c, const char** name) {
+  *name = "cta_scalar_t512";
+  switch (dtype) {
+    case kF32: return launch_scalar_impl<kF32>(p, c);
+    case kF16: return launch_scalar_impl<kF16>(p, c);
+    case kBF16: return launch_scalar_impl<kBF16>(p, c);
+    default: return ADDLN_ERR_DTYPE;
+  }
+}
+
+int read_and_clear_device_error(void* stream, int* code) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ADDLN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return ADDLN_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return ADDLN_ERR_CUDA;
+  *code = v;
+  return ADDLN_OK;
+}
+
+}  // namespace addln

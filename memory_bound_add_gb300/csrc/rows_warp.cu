@@ -1,0 +1,179 @@
+// One warp per row: fused residual add + LayerNorm for short rows (H <= 1024).
+//
+// Each lane loads its share of the row of X and R with 16-byte streaming
+// loads (vector path) or element loads (scalar path, any alignment), adds
+// them in fp32 registers, takes two-pass statistics of its own values, and
+// the warp merges them with a butterfly of Chan updates.  The row never
+// leaves registers: X and R are read once, Y (and optionally A, mean, rstd)
+// written once -- the fused traffic of "算子融合的收益量化" section 1.
+#include "../../include/addln.h"
+#include "common.cuh"
+
+namespace addln {
+
+constexpr int kWarpCtaThreads = 256;  // 8 rows per CTA
+constexpr int kRowsPerCta = kWarpCtaThreads / 32;
+
+template <int DT, int NV, bool VECTOR>
+__global__ void __launch_bounds__(kWarpCtaThreads) k_warp_row(const RowArgs p) {
+  using IO = Io<DT>;
+  constexpr int VEC = VECTOR ? IO::kVec : 1;
+  constexpr int S = IO::kBytes;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
+  if (row >= p.rows) return;  // whole warp leaves together
+  const int H = p.H;
+  const int nvec = H / VEC;
+  const int64_t base = row * static_cast<int64_t>(H);  // element offset of the row
+
+  bool ok[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) ok[k] = (lane + 32 * k) < nvec;
+
+  float v[NV][VEC];
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
+
+  // ---- load X and R once, add in fp32
+  if constexpr (VECTOR) {
+    const char* xrow = static_cast<const char*>(p.x) + base * S;
+    uint4 xv[NV], rv[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (ok[k]) xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(lane + 32 * k) * 16);
+    if (p.r != nullptr) {
+      const char* rrow = static_cast<const char*>(p.r) + base * S;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (ok[k]) rv[k] = ld_stream_v4(rrow + static_cast<int64_t>(lane + 32 * k) * 16);
+    }
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (ok[k]) {
+        IO::unpack(xv[k], v[k]);
+        if (p.r != nullptr) {
+          float t[VEC];
+          IO::unpack(rv[k], t);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) v[k][e] += t[e];
+        }
+      }
+    }
+  } else {
+    float t[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (ok[k]) v[k][0] = IO::load1(p.x, base + lane + 32 * k);
+    if (p.r != nullptr) {
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (ok[k]) t[k] = IO::load1(p.r, base + lane + 32 * k);
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (ok[k]) v[k][0] += t[k];
+    }
+  }
+
+  // ---- row statistics: per-lane two-pass, warp Chan butterfly
+  Stats st = thread_stats<NV, VEC>(v, ok);
+  st = warp_allreduce(st, lane);
+  const float mean = st.m;
+  const float rstd = row_rstd(st, H, p.eps);
+
+  // ---- normalise + affine, store
+  if constexpr (VECTOR) {
+    char* yrow = static_cast<char*>(p.y) + base * S;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (ok[k]) {
+        const int c = lane + 32 * k;
+        float o[VEC];
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+          const float4 g = ld_param_f4(p.gamma + c * VEC + 4 * q);
+          const float4 b = ld_param_f4(p.beta + c * VEC + 4 * q);
+          o[4 * q + 0] = fmaf((v[k][4 * q + 0] - mean) * rstd, g.x, b.x);
+          o[4 * q + 1] = fmaf((v[k][4 * q + 1] - mean) * rstd, g.y, b.y);
+          o[4 * q + 2] = fmaf((v[k][4 * q + 2] - mean) * rstd, g.z, b.z);
+          o[4 * q + 3] = fmaf((v[k][4 * q + 3] - mean) * rstd, g.w, b.w);
+        }
+        st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::pack(o));
+      }
+    }
+    if (p.a != nullptr) {
+      char* arow = static_cast<char*>(p.a) + base * S;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (ok[k]) st_stream_v4(arow + static_cast<int64_t>(lane + 32 * k) * 16, IO::pack(v[k]));
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (ok[k]) {
+        const int j = lane + 32 * k;
+        const float g = __ldg(p.gamma + j), b = __ldg(p.beta + j);
+        IO::store1(p.y, base + j, fmaf((v[k][0] - mean) * rstd, g, b));
+      }
+    }
+    if (p.a != nullptr) {
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (ok[k]) IO::store1(p.a, base + lane + 32 * k, v[k][0]);
+    }
+  }
+  if (lane == 0) {
+    if (p.mean != nullptr) p.mean[row] = mean;
+    if (p.rstd != nullptr) p.rstd[row] = rstd;
+  }
+}
+
+template <int DT, int NV, bool VECTOR>
+static int launch(const RowArgs& p, const LaunchCtx& c) {
+  const int64_t blocks = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
+  if (blocks > 0x7fffffff) return ADDLN_ERR_UNSUPPORTED;
+  k_warp_row<DT, NV, VECTOR>
+      <<<static_cast<unsigned>(blocks), kWarpCtaThreads, 0, static_cast<cudaStream_t>(c.stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+}
+
+// Per-lane slot counts instantiated; the dispatcher takes the smallest that
+// covers the row.
+template <int DT>
+static int launch_vec(const RowArgs& p, const LaunchCtx& c, const char** name) {
+  constexpr int VEC = Io<DT>::kVec;
+  const int nv = (p.H / VEC + 31) / 32;
+  if (nv <= 1) { *name = "warp_vec_nv1"; return launch<DT, 1, true>(p, c); }
+  if (nv <= 2) { *name = "warp_vec_nv2"; return launch<DT, 2, true>(p, c); }
+  if (nv <= 3) { *name = "warp_vec_nv3"; return launch<DT, 3, true>(p, c); }
+  if (nv <= 4) { *name = "warp_vec_nv4"; return launch<DT, 4, true>(p, c); }
+  if constexpr (VEC == 4) {
+    if (nv <= 6) { *name = "warp_vec_nv6"; return launch<DT, 6, true>(p, c); }
+    if (nv <= 8) { *name = "warp_vec_nv8"; return launch<DT, 8, true>(p, c); }
+  }
+  return ADDLN_ERR_UNSUPPORTED;
+}
+
+template <int DT>
+static int launch_scalar(const RowArgs& p, const LaunchCtx& c, const char** name) {
+  const int nv = (p.H + 31) / 32;
+  if (nv <= 2) { *name = "warp_scalar_nv2"; return launch<DT, 2, false>(p, c); }
+  if (nv <= 4) { *name = "warp_scalar_nv4"; return launch<DT, 4, false>(p, c); }
+  if (nv <= 8) { *name = "warp_scalar_nv8"; return launch<DT, 8, false>(p, c); }
+  if (nv <= 16) { *name = "warp_scalar_nv16"; return launch<DT, 16, false>(p, c); }
+  if (nv <= 32) { *name = "warp_scalar_nv32"; return launch<DT, 32, false>(p, c); }
+  return ADDLN_ERR_UNSUPPORTED;
+}
+
+int launch_warp_row(int dtype, bool vec, const RowArgs& p, const LaunchCtx& c,
+                    const char** name) {
+  switch (dtype) {
+    case kF32: return vec ? launch_vec<kF32>(p, c, name) : launch_scalar<kF32>(p, c, name);
+    case kF16: return vec ? launch_vec<kF16>(p, c, name) : launch_scalar<kF16>(p, c, name);
+    case kBF16: return vec ? launch_vec<kBF16>(p, c, name) : launch_scalar<kBF16>(p, c, name);
+    default: return ADDLN_ERR_DTYPE;
+  }
+}
+
+}  // namespace addln

@@ -1,0 +1,84 @@
+"""Tolerances and comparison helpers for GPU-vs-oracle parity tests.
+
+Bounds, all against the fp64 oracle:
+  Y fp32           |dy| <= 1e-5 * (1 + |y|)
+  Y fp16 / bf16    |dy| <= max(4e-3 / 3e-2, ulp_dtype(|y|))
+                   The stated absolute bounds lie below the format's own
+                   rounding step at large |y| (bf16 spacing is 0.0625 on
+                   [8, 16)), so a faithfully rounded value -- within one unit
+                   in the last place of the exact result -- also passes.
+  A (resid_out)    bit-exact: the exact sum rounded to nearest-even in dtype
+  mean             |dmean| <= 1e-5 * (|mean| + sqrt(var + eps))
+                   (relative to the row's scale: a row mean near 0 would make
+                   a plain relative bound meaningless)
+  rstd             |drstd| <= 1e-5 * rstd
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+Y_TOL = {"fp32": 1e-5, "fp16": 4e-3, "bf16": 3e-2}
+PRECISION = {"fp32": 24, "fp16": 11, "bf16": 8}
+MIN_NORMAL_EXP = {"fp32": -126, "fp16": -14, "bf16": -126}
+STAT_TOL = 1e-5
+
+
+def ulp(v: np.ndarray, dtype: str) -> np.ndarray:
+    """Spacing of ``dtype`` values at |v| (subnormal spacing below the normals)."""
+    p = PRECISION[dtype]
+    av = np.abs(v)
+    lo = MIN_NORMAL_EXP[dtype]
+    with np.errstate(divide="ignore"):
+        e = np.where(av > 0, np.floor(np.log2(np.where(av > 0, av, 1.0))), lo)
+    e = np.maximum(e, lo)
+    return np.ldexp(1.0, (e - p + 1).astype(np.int64))
+
+
+def to_f64(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        return t.detach().cpu().double().numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def y_violations(y_gpu, y_ref: np.ndarray, dtype: str) -> np.ndarray:
+    """Boolean mask of Y elements outside the bound."""
+    yg = to_f64(y_gpu)
+    err = np.abs(yg - y_ref)
+    if dtype == "fp32":
+        bound = Y_TOL["fp32"] * (1 + np.abs(y_ref))
+    else:
+        bound = np.maximum(Y_TOL[dtype], ulp(y_ref, dtype))
+    return ~(err <= bound)
+
+
+def assert_y(y_gpu, y_ref, dtype, what=""):
+    bad = y_violations(y_gpu, y_ref, dtype)
+    if bad.any():
+        yg = to_f64(y_gpu)
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} Y elements out of bound; first "
+            + ", ".join(f"{tuple(i)} gpu={yg[tuple(i)]!r} ref={y_ref[tuple(i)]!r}" for i in idx))
+
+
+def assert_a(a_gpu, a_ref, what=""):
+    ag = to_f64(a_gpu)
+    same = (ag == a_ref) | (np.isnan(ag) & np.isnan(a_ref))
+    if not same.all():
+        idx = np.argwhere(~same)[:5]
+        raise AssertionError(
+            f"{what}: {int((~same).sum())} A elements differ from the rounded sum; first "
+            + ", ".join(f"{tuple(i)} gpu={ag[tuple(i)]!r} ref={a_ref[tuple(i)]!r}" for i in idx))
+
+
+def assert_stats(mean_gpu, rstd_gpu, mean_ref, rstd_ref, what=""):
+    mg, rg = to_f64(mean_gpu), to_f64(rstd_gpu)
+    scale = np.abs(mean_ref) + 1.0 / rstd_ref
+    badm = ~(np.abs(mg - mean_ref) <= STAT_TOL * scale)
+    badr = ~(np.abs(rg - rstd_ref) <= STAT_TOL * rstd_ref)
+    if badm.any() or badr.any():
+        i = int(np.argmax(badm | badr))
+        raise AssertionError(
+            f"{what}: {int(badm.sum())} mean / {int(badr.sum())} rstd out of bound; row {i}: "
+            f"mean gpu={mg[i]!r} ref={mean_ref[i]!r}, rstd gpu={rg[i]!r} ref={rstd_ref[i]!r}")

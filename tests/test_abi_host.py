@@ -1,0 +1,208 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+The library must load on a machine without a GPU, export every symbol
+include/addln.h declares, and reject bad arguments before its first CUDA
+call.  Pointers below are fake addresses: every call here fails validation,
+so none is ever dereferenced.
+"""
+from __future__ import annotations
+
+import os
+import re
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "addln.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from memory_bound_add_gb300.build import build
+    build()
+    from memory_bound_add_gb300 import binding
+    return binding.lib()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def header_defines():
+    vals = {}
+    for m in re.finditer(r"#define\s+(ADDLN_\w+)\s+\(?(-?\d+)\)?", open(HEADER).read()):
+        vals[m.group(1)] = int(m.group(2))
+    return vals
+
+
+def test_header_declares_the_expected_entry_points():
+    assert header_functions() == sorted([
+        "add_layernorm_fwd", "add_fwd", "layernorm_fwd", "addln_strerror", "addln_max_hidden",
+        "addln_get_device_error", "addln_set_force_path", "addln_set_wait_limit_ns",
+        "addln_set_grid_cap", "addln_last_path"])
+
+
+def test_library_exports_every_header_symbol(lib):
+    from memory_bound_add_gb300.build import LIB
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in header_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_binding_signatures_cover_the_header():
+    from memory_bound_add_gb300 import binding
+    assert sorted(binding.SIGNATURES) == header_functions()
+    d = header_defines()
+    assert (binding.FP32, binding.FP16, binding.BF16) == (d["ADDLN_FP32"], d["ADDLN_FP16"],
+                                                          d["ADDLN_BF16"])
+    for k in ("NULL", "SHAPE", "DTYPE", "EPS", "ALIAS", "LAUNCH", "UNSUPPORTED",
+              "DEVICE_TIMEOUT", "CUDA"):
+        assert getattr(binding, "ERR_" + k) == d["ADDLN_ERR_" + k]
+    for k in ("AUTO", "WARP_VEC", "CTA_TMA", "CTA_VEC", "SCALAR"):
+        assert getattr(binding, "PATH_" + k) == d["ADDLN_PATH_" + k]
+
+
+def test_strerror_and_limits(lib):
+    from memory_bound_add_gb300 import binding as b
+    for code in range(-9, 1):
+        assert lib.addln_strerror(code)
+    assert b"unknown" in lib.addln_strerror(-99)
+    assert lib.addln_max_hidden(b.FP32) == 16384
+    assert lib.addln_max_hidden(b.FP16) == 32768
+    assert lib.addln_max_hidden(b.BF16) == 32768
+    assert lib.addln_max_hidden(7) == b.ERR_DTYPE
+    assert lib.addln_last_path() == b"none"
+
+
+def test_force_path_setter(lib):
+    from memory_bound_add_gb300 import binding as b
+    assert lib.addln_set_force_path(b.PATH_SCALAR) == b.PATH_AUTO
+    assert lib.addln_set_force_path(b.PATH_AUTO) == b.PATH_SCALAR
+    assert lib.addln_set_force_path(99) == b.ERR_SHAPE
+    assert lib.addln_set_wait_limit_ns(5) == 1000000000
+    assert lib.addln_set_wait_limit_ns(1000000000) == 5
+    assert lib.addln_set_grid_cap(3) == 0
+    assert lib.addln_set_grid_cap(0) == 3
+
+
+BASE = 0x7F0000000000   # fake, 16-byte aligned
+
+
+def fused(lib, x=BASE, r=BASE + 0x1000000, g=BASE + 0x2000000, bt=BASE + 0x2100000,
+          y=BASE + 0x3000000, a=None, mean=None, rstd=None, rows=4, H=8, eps=1e-5, dtype=0):
+    return lib.add_layernorm_fwd(x, r, g, bt, y, a, mean, rstd, rows, H, eps, dtype, None)
+
+
+def test_validation_codes(lib):
+    from memory_bound_add_gb300 import binding as b
+    assert fused(lib, dtype=3) == b.ERR_DTYPE
+    assert fused(lib, dtype=-1) == b.ERR_DTYPE
+    assert fused(lib, H=0) == b.ERR_SHAPE
+    assert fused(lib, H=-5) == b.ERR_SHAPE
+    assert fused(lib, rows=-1) == b.ERR_SHAPE
+    assert fused(lib, H=16385, dtype=b.FP32) == b.ERR_SHAPE
+    assert fused(lib, H=32769, dtype=b.BF16) == b.ERR_SHAPE
+    assert fused(lib, rows=(1 << 62), H=8) == b.ERR_SHAPE
+    assert fused(lib, eps=-1e-6) == b.ERR_EPS
+    assert fused(lib, eps=float("nan")) == b.ERR_EPS
+    assert fused(lib, eps=float("inf")) == b.ERR_EPS
+    assert fused(lib, x=None) == b.ERR_NULL
+    assert fused(lib, r=None) == b.ERR_NULL
+    assert fused(lib, g=None) == b.ERR_NULL
+    assert fused(lib, bt=None) == b.ERR_NULL
+    assert fused(lib, y=None) == b.ERR_NULL
+    # rows == 0 is a no-op once dtype, H and eps are valid, even with NULLs
+    assert fused(lib, rows=0, x=None, y=None) == b.OK
+    assert fused(lib, rows=0, dtype=9) == b.ERR_DTYPE
+
+
+def test_alias_rules(lib):
+    from memory_bound_add_gb300 import binding as b
+    rows, H = 4, 8
+    tb = rows * H * 4
+    x = BASE
+    # partial overlaps of an output with an input
+    assert fused(lib, x=x, y=x + 16) == b.ERR_ALIAS
+    assert fused(lib, x=x, y=x - 16) == b.ERR_ALIAS
+    assert fused(lib, r=x + 0x1000000, a=x + 0x1000000 + 32, y=x + 0x3000000) == b.ERR_ALIAS
+    # output over gamma or beta, even exactly
+    assert fused(lib, y=BASE + 0x2000000) == b.ERR_ALIAS
+    assert fused(lib, mean=BASE + 0x2100000 + 4, rstd=BASE + 0x5000000) == b.ERR_ALIAS
+    # outputs against each other
+    y = BASE + 0x3000000
+    assert fused(lib, y=y, a=y) == b.ERR_ALIAS
+    assert fused(lib, y=y, a=y + tb - 16) == b.ERR_ALIAS
+    m = BASE + 0x6000000
+    assert fused(lib, mean=m, rstd=m + 8) == b.ERR_ALIAS
+    assert fused(lib, mean=m, rstd=y + 64) == b.ERR_ALIAS
+    # the unfused kernels
+    assert lib.add_fwd(x, x + 0x1000000, x + 8, 64, 0, None) == b.ERR_ALIAS
+    assert lib.add_fwd(x, None, x + 0x4000000, 64, 0, None) == b.ERR_NULL
+    assert lib.add_fwd(x, x, x, -1, 0, None) == b.ERR_SHAPE
+    assert lib.add_fwd(x, x, x, 64, 5, None) == b.ERR_DTYPE
+    assert lib.add_fwd(None, None, None, 0, 0, None) == b.OK
+    assert lib.layernorm_fwd(x, BASE + 0x2000000, BASE + 0x2100000, x + 4, None, None, rows, H,
+                             1e-5, 0, None) == b.ERR_ALIAS
+    assert lib.layernorm_fwd(x, None, BASE + 0x2100000, y, None, None, rows, H, 1e-5, 0,
+                             None) == b.ERR_NULL
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "from memory_bound_add_gb300 import binding\n"
+        "binding.LIB_PATH = %r\n"
+        "try:\n"
+        "    binding.lib()\n"
+        "except RuntimeError as e:\n"
+        "    print('raised', e)\n"
+        "else:\n"
+        "    print('loaded')\n" % (ROOT, str(tmp_path / "nope.so")))
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, check=True)
+    assert out.stdout.startswith("raised")
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "memory_bound_add_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle", text, flags=re.M), f
+                assert "liboracle" not in text and "addln_oracle" not in text, f
+    for f in ("addln.h",):
+        assert "oracle" not in open(os.path.join(ROOT, "include", f)).read()
+
+
+def test_oracle_shares_no_code_with_the_library():
+    src = open(os.path.join(ROOT, "oracle", "addln_oracle.c")).read()
+    assert "#include \"" not in src          # only system headers
+    for dirpath, _, files in os.walk(os.path.join(ROOT, "oracle")):
+        for f in files:
+            if f.endswith(".py"):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "memory_bound_add_gb300" not in text, f
+
+
+def test_tolerance_helper_ulp():
+    sys.path.insert(0, os.path.dirname(__file__))
+    from _parity import ulp, y_violations
+    assert ulp(np.array([1.0]), "bf16")[0] == 2.0 ** -7
+    assert ulp(np.array([10.0]), "bf16")[0] == 2.0 ** -4
+    assert ulp(np.array([1.0]), "fp16")[0] == 2.0 ** -10
+    assert ulp(np.array([0.0]), "fp16")[0] == 2.0 ** -24
+    ref = np.array([10.03])
+    assert not y_violations(np.array([10.0625]), ref, "bf16").any()   # one rounding step away
+    assert y_violations(np.array([10.25]), ref, "bf16").any()
+    assert y_violations(np.array([1.0 + 5e-3]), np.array([1.0]), "fp16").any()
+    assert not y_violations(np.array([1.0 + 1e-5]), np.array([1.0]), "fp32").any()
+    assert y_violations(np.array([1.0 + 3e-5]), np.array([1.0]), "fp32").any()

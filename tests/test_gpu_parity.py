@@ -1,0 +1,341 @@
+"""GPU parity: the CUDA kernels (called through the C ABI) against the fp64
+oracle on the same seeded inputs.
+
+Small cases run every kernel path, every output combination and a ragged
+tail of rows; the persistent CTA kernels also run with a capped grid so each
+CTA walks many rows through its two-stage copy pipeline.  Full-size
+workloads run in the launch configuration the benchmark times and are
+checked on sampled rows, plus every special row (constant rows, outliers).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _parity import assert_a, assert_stats, assert_y
+
+pytestmark = pytest.mark.gpu
+
+mba = pytest.importorskip("memory_bound_add_gb300")
+
+PATHS = {
+    "auto": 0,
+    "warp_vec": 1,
+    "cta_tma": 2,
+    "cta_vec": 3,
+    "scalar": 4,
+}
+TD = synth.TORCH_DTYPES
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from memory_bound_add_gb300.build import build
+    build()
+    mba.addln_set_force_path(0)
+    mba.addln_set_grid_cap(0)
+    yield
+    mba.addln_set_force_path(0)
+    mba.addln_set_grid_cap(0)
+
+
+def _dev(d):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def run_fused(d, path=0, want_a=True, want_stats=True, grid_cap=0, inplace=None):
+    """One add_layernorm_fwd call on device copies of d's inputs."""
+    g = _dev(d)
+    x, r = g["x"], g["r"]
+    rows = x.shape[0]
+    y = torch.empty_like(x)
+    a = torch.empty_like(x) if want_a else None
+    mean = torch.empty(rows, dtype=torch.float32, device="cuda") if want_stats else None
+    rstd = torch.empty(rows, dtype=torch.float32, device="cuda") if want_stats else None
+    if inplace == "y=x":
+        y = x
+    elif inplace == "a=r":
+        a = r
+    prev = mba.addln_set_force_path(path)
+    prev_cap = mba.addln_set_grid_cap(grid_cap)
+    try:
+        mba.add_layernorm_fwd(x, r, g["gamma"], g["beta"], y, a, mean, rstd, eps=g["eps"])
+        name = mba.addln_last_path()
+        torch.cuda.synchronize()
+    finally:
+        mba.addln_set_force_path(prev)
+        mba.addln_set_grid_cap(prev_cap)
+    assert mba.addln_get_device_error() == 0
+    out = {"y": y.cpu(), "a": a.cpu() if a is not None else None,
+           "mean": mean.cpu() if mean is not None else None,
+           "rstd": rstd.cpu() if rstd is not None else None, "path": name}
+    return out
+
+
+def check(w, d, out, what, rows=None):
+    x, r = d["x"], d["r"]
+    if rows is not None:
+        x, r = x[rows], r[rows]
+    ref = oracle.oracle_add_layernorm(x, r, d["gamma"], d["beta"], d["eps"], w.dtype)
+    sel = (lambda t: t[rows]) if rows is not None else (lambda t: t)
+    assert_y(sel(out["y"]), ref["y"], w.dtype, what)
+    if out["a"] is not None:
+        assert_a(sel(out["a"]), ref["a"], what)
+    if out["mean"] is not None:
+        assert_stats(sel(out["mean"]), sel(out["rstd"]), ref["mean"], ref["rstd"], what)
+    return ref
+
+
+def _supported(path, w):
+    vec_ok = (w.H * w.elem_bytes) % 16 == 0
+    if path == "warp_vec":
+        return vec_ok and w.H <= 1024
+    if path in ("cta_tma", "cta_vec"):
+        return vec_ok
+    return True
+
+
+# ------------------------------------------------------------- small cases
+SMALL_ROWS = 301  # not a multiple of the 8 rows a warp-per-row CTA covers
+
+
+@pytest.mark.parametrize("name", synth.PRIMARY + synth.TAILS)
+@pytest.mark.parametrize("path", list(PATHS))
+def test_small_all_paths(name, path):
+    w = synth.with_rows(synth.get(name), SMALL_ROWS)
+    if not _supported(path, w):
+        pytest.skip("path cannot run this row layout")
+    d = synth.make_inputs(w, seed=1)
+    out = run_fused(d, PATHS[path])
+    check(w, d, out, f"{name}/{path}/{out['path']}")
+
+
+@pytest.mark.parametrize("name", ["pages_2048x4096_fp16", "large_32768x8192_bf16",
+                                  "tail_4096x1002_fp32", "cancel_65536x1000_bf16"])
+@pytest.mark.parametrize("path", ["cta_tma", "cta_vec", "scalar"])
+@pytest.mark.parametrize("cap", [1, 7, 19])
+def test_persistent_grid_walks_many_rows(name, path, cap):
+    w = synth.with_rows(synth.get(name), 150)
+    if not _supported(path, w):
+        pytest.skip("path cannot run this row layout")
+    if path == "scalar" and w.H <= 1024:
+        pytest.skip("scalar path is warp-per-row at this H")
+    d = synth.make_inputs(w, seed=2)
+    out = run_fused(d, PATHS[path], grid_cap=cap)
+    check(w, d, out, f"{name}/{path}/cap{cap}")
+
+
+@pytest.mark.parametrize("want_a,want_stats", [(False, False), (True, False), (False, True)])
+@pytest.mark.parametrize("name", ["tiny_64x768_fp32", "pages_2048x4096_fp16",
+                                  "tail_4096x999_bf16"])
+def test_output_combinations(name, want_a, want_stats):
+    w = synth.with_rows(synth.get(name), 77)
+    d = synth.make_inputs(w, seed=3)
+    out = run_fused(d, 0, want_a=want_a, want_stats=want_stats)
+    check(w, d, out, f"{name}/a{int(want_a)}s{int(want_stats)}")
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+@pytest.mark.parametrize("H", [1, 2, 7, 8, 9, 31, 32, 33, 255, 257, 1000, 1001, 1023, 1024, 1025,
+                               2048, 4095, 4097, 8192, 12288])
+@pytest.mark.parametrize("rows", [1, 3, 33])
+def test_shape_sweep(dtype, H, rows):
+    w = synth.custom(rows, H, dtype, x_dist=(3.0, 2.0), want_resid=True, want_stats=True)
+    d = synth.make_inputs(w, seed=H * 7 + rows)
+    out = run_fused(d, 0)
+    check(w, d, out, f"{rows}x{H} {dtype} {out['path']}")
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+def test_maximum_hidden(dtype):
+    H = mba.addln_max_hidden(mba.binding.DTYPE_CODE[TD[dtype]])
+    w = synth.custom(5, H, dtype, want_resid=True, want_stats=True)
+    d = synth.make_inputs(w, seed=4)
+    for path in ("auto", "scalar"):
+        out = run_fused(d, PATHS[path])
+        check(w, d, out, f"maxH {dtype} {path} {out['path']}")
+
+
+def test_hidden_above_maximum_is_rejected():
+    H = mba.addln_max_hidden(mba.BF16) + 8
+    x = torch.zeros(2, H, dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(H, device="cuda")
+    with pytest.raises(mba.AddLNError) as e:
+        mba.add_layernorm(x, x.clone(), g, g.clone())
+    assert e.value.code == mba.binding.ERR_SHAPE
+
+
+# ---------------------------------------------------------------- edge cases
+@pytest.mark.parametrize("name", ["tiny_64x768_fp32", "pages_2048x4096_fp16",
+                                  "tail_4096x1001_bf16"])
+@pytest.mark.parametrize("mode", ["y=x", "a=r"])
+def test_in_place(name, mode):
+    w = synth.with_rows(synth.get(name), 40)
+    d = synth.make_inputs(w, seed=5)
+    out = run_fused(d, 0, inplace=mode)
+    check(w, d, out, f"{name} in place {mode}")
+
+
+@pytest.mark.parametrize("dtype,H", [("bf16", 4096), ("fp16", 768), ("fp32", 2048)])
+def test_misaligned_pointers_take_element_path(dtype, H):
+    rows = 37
+    w = synth.custom(rows, H, dtype, want_resid=True, want_stats=True)
+    d = synth.make_inputs(w, seed=6)
+    n = rows * H
+    xb = torch.empty(n + 8, dtype=TD[dtype], device="cuda")
+    rb = torch.empty(n + 8, dtype=TD[dtype], device="cuda")
+    x = xb[1:1 + n].view(rows, H)
+    r = rb[1:1 + n].view(rows, H)
+    x.copy_(d["x"].cuda())
+    r.copy_(d["r"].cuda())
+    y = torch.empty_like(x)
+    a = torch.empty_like(x)
+    mean = torch.empty(rows, device="cuda")
+    rstd = torch.empty(rows, device="cuda")
+    g, b = d["gamma"].cuda(), d["beta"].cuda()
+    prev = mba.addln_set_force_path(mba.PATH_CTA_TMA)
+    try:
+        with pytest.raises(mba.AddLNError) as e:
+            mba.add_layernorm_fwd(x, r, g, b, y, a, mean, rstd, eps=d["eps"])
+        assert e.value.code == mba.binding.ERR_UNSUPPORTED
+    finally:
+        mba.addln_set_force_path(prev)
+    mba.add_layernorm_fwd(x, r, g, b, y, a, mean, rstd, eps=d["eps"])
+    assert "scalar" in mba.addln_last_path()
+    torch.cuda.synchronize()
+    out = {"y": y.cpu(), "a": a.cpu(), "mean": mean.cpu(), "rstd": rstd.cpu()}
+    check(w, d, out, f"misaligned {dtype} {H}")
+
+
+def test_zero_rows_is_a_noop():
+    x = torch.empty(0, 768, dtype=torch.float16, device="cuda")
+    g = torch.ones(768, device="cuda")
+    y, _, _, _ = mba.add_layernorm(x, x, g, g)
+    assert y.shape == (0, 768)
+
+
+@pytest.mark.parametrize("name", ["tiny_64x768_fp32", "pages_2048x4096_fp16",
+                                  "tail_4096x999_bf16", "large_32768x8192_bf16"])
+def test_outputs_do_not_write_outside_their_rows(name):
+    w = synth.with_rows(synth.get(name), 21)
+    d = synth.make_inputs(w, seed=7)
+    g = _dev(d)
+    rows, H = w.rows, w.H
+    pad = 128
+    sentinel = -12345.0
+    ybuf = torch.full((rows * H + 2 * pad,), sentinel, dtype=TD[w.dtype], device="cuda")
+    abuf = torch.full((rows * H + 2 * pad,), sentinel, dtype=TD[w.dtype], device="cuda")
+    sbuf = torch.full((2 * rows + 4 * pad,), sentinel, dtype=torch.float32, device="cuda")
+    y = ybuf[pad:pad + rows * H].view(rows, H)
+    a = abuf[pad:pad + rows * H].view(rows, H)
+    mean = sbuf[pad:pad + rows]
+    rstd = sbuf[3 * pad + rows:3 * pad + 2 * rows]
+    mba.add_layernorm_fwd(g["x"], g["r"], g["gamma"], g["beta"], y, a, mean, rstd, eps=g["eps"])
+    torch.cuda.synchronize()
+    for buf in (ybuf, abuf):
+        assert torch.all(buf[:pad] == sentinel) and torch.all(buf[-pad:] == sentinel)
+    assert torch.all(sbuf[:pad] == sentinel)
+    assert torch.all(sbuf[pad + rows:3 * pad + rows] == sentinel)
+    assert torch.all(sbuf[3 * pad + 2 * rows:] == sentinel)
+    out = {"y": y.cpu(), "a": a.cpu(), "mean": mean.cpu(), "rstd": rstd.cpu()}
+    check(w, d, out, f"{name} canary")
+
+
+def test_constant_rows_are_exact():
+    # a constant row: mean is the constant, the variance 0, and Y is beta
+    # rounded to the dtype, on every kernel path
+    w = synth.with_rows(synth.get("cancel_65536x1000_bf16"), 400)
+    d = synth.make_inputs(w, seed=8)
+    cr = d["const_rows"]
+    assert len(cr) == 4
+    for path in ("auto", "cta_tma", "cta_vec", "scalar"):
+        out = run_fused(d, PATHS[path])
+        beta_bf16 = d["beta"].to(torch.bfloat16)
+        for i in cr:
+            assert torch.equal(out["y"][i], beta_bf16), path
+            assert out["mean"][i].item() == d["x"][i, 0].float().item(), path
+        check(w, d, out, f"constant rows {path}")
+
+
+def test_deterministic_bitwise():
+    w = synth.with_rows(synth.get("large_32768x8192_bf16"), 200)
+    d = synth.make_inputs(w, seed=9)
+    o1 = run_fused(d, 0)
+    o2 = run_fused(d, 0)
+    assert torch.equal(o1["y"], o2["y"]) and torch.equal(o1["a"], o2["a"])
+
+
+# ------------------------------------------------------- unfused baseline
+@pytest.mark.parametrize("name", synth.PRIMARY + synth.TAILS)
+def test_unfused_chain_matches_oracle_with_rounded_A(name):
+    w = synth.with_rows(synth.get(name), 129)
+    d = synth.make_inputs(w, seed=10)
+    g = _dev(d)
+    y, a, mean, rstd = mba.add_then_layernorm(g["x"], g["r"], g["gamma"], g["beta"], eps=g["eps"],
+                                              want_stats=True)
+    torch.cuda.synchronize()
+    ref = oracle.oracle_add_layernorm(d["x"], d["r"], d["gamma"], d["beta"], d["eps"], w.dtype,
+                                      round_A=True)
+    assert_a(a.cpu(), ref["a"], f"{name} unfused A")
+    assert_y(y.cpu(), ref["y"], w.dtype, f"{name} unfused Y")
+    assert_stats(mean.cpu(), rstd.cpu(), ref["mean"], ref["rstd"], f"{name} unfused stats")
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+@pytest.mark.parametrize("n", [1, 7, 8, 4097, 1 << 20, (1 << 20) + 3])
+def test_add_kernel(dtype, n):
+    g = torch.Generator().manual_seed(n)
+    x = (torch.randn(n, generator=g) * 3).to(TD[dtype])
+    r = torch.randn(n, generator=g).to(TD[dtype])
+    a = torch.empty_like(x, device="cuda")
+    mba.add_fwd(x.cuda(), r.cuda(), a)
+    torch.cuda.synchronize()
+    assert_a(a.cpu(), oracle.oracle_add(x, r, dtype, round_A=True), f"add {dtype} {n}")
+
+
+# -------------------------------------------------------- bounded waits
+def test_wait_timeout_sets_device_error_and_recovers():
+    w = synth.with_rows(synth.get("pages_2048x4096_fp16"), 64)
+    d = synth.make_inputs(w, seed=11)
+    g = _dev(d)
+    y = torch.empty_like(g["x"])
+    prev_path = mba.addln_set_force_path(mba.PATH_CTA_TMA)
+    prev_limit = mba.addln_set_wait_limit_ns(0)
+    try:
+        mba.add_layernorm_fwd(g["x"], g["r"], g["gamma"], g["beta"], y, eps=g["eps"])
+        assert mba.addln_get_device_error() == mba.binding.ERR_DEVICE_TIMEOUT
+    finally:
+        mba.addln_set_wait_limit_ns(prev_limit)
+        mba.addln_set_force_path(prev_path)
+    assert mba.addln_get_device_error() == 0        # read-and-clear
+    out = run_fused(d, 0, want_a=False, want_stats=False)
+    check(w, d, out, "after timeout")
+
+
+# ------------------------------------------------------------ full sizes
+def _sample_rows(w, d, n=192, seed=0):
+    g = np.random.default_rng(seed)
+    rows = set(range(min(32, w.rows))) | set(range(max(0, w.rows - 32), w.rows))
+    rows |= set(g.choice(w.rows, size=min(n, w.rows), replace=False).tolist())
+    rows |= set(d["const_rows"].tolist())
+    if len(d["outlier_pos"]):
+        rows |= set((d["outlier_pos"][:: max(1, len(d["outlier_pos"]) // 64)] // w.H).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", synth.PRIMARY + synth.TAILS)
+def test_full_size_sampled_rows(name):
+    w = synth.get(name)
+    d = synth.make_inputs(w, seed=0)
+    out = run_fused(d, 0, want_a=w.want_resid, want_stats=w.want_stats)
+    rows = _sample_rows(w, d)
+    check(w, d, out, f"{name} full size ({out['path']}), {len(rows)} sampled rows", rows=rows)
+    assert torch.isfinite(out["y"]).all()
+    for i in d["const_rows"]:
+        assert torch.equal(out["y"][i], d["beta"].to(TD[w.dtype]))
