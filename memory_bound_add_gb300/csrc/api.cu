@@ -173,7 +173,8 @@ int add_layernorm_fwd(const void* x, const void* r, const float* gamma, const fl
                       float eps, int dtype, void* stream) {
   int rc = check_rows_args(x, r, true, gamma, beta, y, resid_out, mean, rstd, rows, H, eps, dtype);
   if (rc != ADDLN_OK || rows == 0) return rc;
-  RowArgs p{x, r, gamma, beta, y, resid_out, mean, rstd, rows, static_cast<int>(H), eps,
+  RowArgs p{x, r, gamma, beta, y, resid_out, mean, rstd, rows, static_cast<int>(H),
+            static_cast<float>(1.0 / static_cast<double>(H)), eps,
             g_wait_limit_ns.load(std::memory_order_relaxed)};
   return run_rows(p, dtype, stream);
 }
@@ -183,7 +184,8 @@ int layernorm_fwd(const void* a, const float* gamma, const float* beta, void* y,
   int rc = check_rows_args(a, nullptr, false, gamma, beta, y, nullptr, mean, rstd, rows, H, eps,
                            dtype);
   if (rc != ADDLN_OK || rows == 0) return rc;
-  RowArgs p{a, nullptr, gamma, beta, y, nullptr, mean, rstd, rows, static_cast<int>(H), eps,
+  RowArgs p{a, nullptr, gamma, beta, y, nullptr, mean, rstd, rows, static_cast<int>(H),
+            static_cast<float>(1.0 / static_cast<double>(H)), eps,
             g_wait_limit_ns.load(std::memory_order_relaxed)};
   return run_rows(p, dtype, stream);
 }

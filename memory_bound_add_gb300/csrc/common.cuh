@@ -6,10 +6,10 @@
 // The statistics follow the LayerNorm of "算子融合与Kernel合并" 4.2 (mean,
 // then the biased variance around it, eps inside the square root) but are
 // gathered in one pass over registers: each thread takes the exact two-pass
-// mean/M2 of the values it holds, and partial results are merged with Chan,
-// Golub and LeVeque's pairwise update.  The page's own one-pass shortcut
-// (sum and sum of squares, same page 4.3) is avoided: it cancels when the
-// row mean is large against its spread.
+// mean/M2 of the values it holds (shifted by the row's first value), and
+// partial results are merged with Chan, Golub and LeVeque's pairwise update.  The
+// page's own one-pass shortcut (sum and sum of squares, same page 4.3) is
+// avoided: it cancels when the row mean is large against its spread.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -210,79 +210,103 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // ------------------------------------------------------------- statistics
-struct Stats {
-  float n;   // element count (exact in fp32 up to 2^24)
-  float m;   // mean
-  float M2;  // sum of squared deviations from m
+// Every thread of a row works on the row's values shifted by one common
+// value K of that row (its first sum a_0): Chan, Golub and LeVeque's
+// "shifted data".  The sums then run at the size of the row's spread, so a
+// row whose mean is large against its standard deviation loses nothing to
+// the mean's magnitude, and a constant row gives exactly m = 0, M2 = 0.
+//
+// A partial covers n of the row's values: m = mean of (a - K), M2 = sum of
+// squared deviations from that mean.
+struct Part {
+  float n;
+  float m;
+  float M2;
 };
 
-// Chan et al. pairwise update.  Not symmetric in rounding, so callers always
-// pass the lower-indexed partial as `a`; every thread then holds bitwise the
-// same totals.  An empty side (n = 0) leaves the other side unchanged.
-__device__ __forceinline__ Stats chan_combine(const Stats& a, const Stats& b) {
-  Stats o;
+// Chan et al.'s pairwise update, written so that merge(a, b) and merge(b, a)
+// give bitwise the same result (only commutative operations on the two
+// sides), so a xor butterfly leaves identical totals in every lane with no
+// broadcast.  EQUAL: both sides hold the same count (the case for every level
+// when each thread holds the same number of values): no division.
+template <bool EQUAL>
+__device__ __forceinline__ Part merge(const Part& a, const Part& b) {
+  Part o;
+  const float d = b.m - a.m;  // squared below, so its sign does not matter
   o.n = a.n + b.n;
-  const float wb = __fdiv_rn(b.n, fmaxf(o.n, 1.0f));
-  const float d = b.m - a.m;
-  o.m = fmaf(d, wb, a.m);
-  o.M2 = fmaf(d * d * a.n, wb, a.M2 + b.M2);
+  if constexpr (EQUAL) {
+    o.m = (a.m + b.m) * 0.5f;
+    o.M2 = fmaf(d * d, a.n * 0.5f, a.M2 + b.M2);
+  } else {
+    const float inv = __frcp_rn(fmaxf(o.n, 1.0f));
+    o.m = (a.n * a.m + b.n * b.m) * inv;
+    o.M2 = fmaf(d * d, (a.n * b.n) * inv, a.M2 + b.M2);
+  }
   return o;
 }
 
-// Butterfly all-reduce over the 32 lanes with a fixed lower/upper order at
-// every level, so all lanes finish with identical (n, m, M2).
-__device__ __forceinline__ Stats warp_allreduce(Stats s, int lane) {
+// All-reduce of partials over groups of WIDTH lanes (xor butterfly).
+template <bool EQUAL, int WIDTH>
+__device__ __forceinline__ Part butterfly(Part p) {
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    Stats o;
-    o.n = __shfl_xor_sync(0xffffffffu, s.n, off);
-    o.m = __shfl_xor_sync(0xffffffffu, s.m, off);
-    o.M2 = __shfl_xor_sync(0xffffffffu, s.M2, off);
-    const bool upper = (lane & off) != 0;
-    const Stats lo = upper ? o : s;
-    const Stats hi = upper ? s : o;
-    s = chan_combine(lo, hi);
+  for (int off = 1; off < WIDTH; off <<= 1) {
+    Part o;
+    o.n = EQUAL ? p.n : __shfl_xor_sync(0xffffffffu, p.n, off);
+    o.m = __shfl_xor_sync(0xffffffffu, p.m, off);
+    o.M2 = __shfl_xor_sync(0xffffffffu, p.M2, off);
+    p = merge<EQUAL>(p, o);
   }
-  return s;
+  return p;
 }
 
-// Two-pass statistics of the values one thread holds: exact mean of its own
-// values (IEEE division, so a constant run gives its value back exactly),
-// then the sum of squared deviations around it.
-template <int NV, int VEC>
-__device__ __forceinline__ Stats thread_stats(const float (&v)[NV][VEC], const bool (&ok)[NV]) {
+// Two-pass statistics of the values one thread holds, relative to the row
+// shift K (pass K = 0.f for values already shifted): the mean of its own
+// values, then the sum of squared deviations around it.  FULL: every slot
+// holds a value (the row divides evenly over the threads).
+template <int NV, int VEC, bool FULL>
+__device__ __forceinline__ Part thread_part(const float (&v)[NV][VEC], const bool (&ok)[NV],
+                                            float K) {
   float sum = 0.f;
   int cnt = 0;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
-    if (ok[k]) {
+    if (FULL || ok[k]) {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) sum += v[k][e];
+      for (int e = 0; e < VEC; ++e) sum += v[k][e] - K;
       cnt += VEC;
     }
   }
-  Stats s;
-  s.n = static_cast<float>(cnt);
-  s.m = cnt ? __fdiv_rn(sum, s.n) : 0.f;
+  Part p;
+  p.n = static_cast<float>(cnt);
+  constexpr int kN = NV * VEC;
+  if constexpr (FULL && (kN & (kN - 1)) == 0)
+    p.m = sum * (1.0f / kN);  // exact: a power of two
+  else
+    p.m = cnt ? __fdiv_rn(sum, p.n) : 0.f;
   float M2 = 0.f;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
-    if (ok[k]) {
+    if (FULL || ok[k]) {
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        const float d = v[k][e] - s.m;
+        const float d = (v[k][e] - K) - p.m;
         M2 = fmaf(d, d, M2);
       }
     }
   }
-  s.M2 = M2;
-  return s;
+  p.M2 = M2;
+  return p;
 }
 
-// rstd = 1 / sqrt(M2 / H + eps), from the row totals.
-__device__ __forceinline__ float row_rstd(const Stats& t, int H, float eps) {
-  const float var = __fdiv_rn(t.M2, static_cast<float>(H));
-  return rsqrtf(var + eps);
+// y = gamma * (a - mean) * rstd + beta with mean = K + m; the deviation is
+// taken as (a - K) - m so it never passes through the rounded absolute mean.
+__device__ __forceinline__ float normalise(float a, float K, float m, float rstd, float g, float b) {
+  return fmaf(((a - K) - m) * rstd, g, b);
+}
+
+// rstd = 1 / sqrt(M2 / H + eps); inv_h = 1/H rounded to fp32.
+__device__ __forceinline__ float row_rstd(float M2, float inv_h, float eps) {
+  return rsqrtf(fmaf(M2, inv_h, eps));
 }
 
 }  // namespace addln

@@ -21,6 +21,7 @@ struct RowArgs {
   float* rstd;
   int64_t rows;
   int H;
+  float inv_h;  // 1/H rounded to fp32
   float eps;
   uint64_t wait_limit_ns;  // bound on mbarrier waits (TMA path)
 };

@@ -33,7 +33,17 @@ __device__ int g_device_error = 0;
 
 constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s
 
-template <int DT, int THREADS, int NV, bool TMA>
+// CTA-level all-reduce of per-warp partials: lane 0 of each warp has put its
+// warp's totals in red[0..NW); every warp reads red[lane % NW] and runs the
+// butterfly over NW lanes, so all threads end with identical row totals.
+template <bool FULL, int NW>
+__device__ __forceinline__ Part cta_totals(const Part* red, int lane) {
+  Part q = red[lane % NW];
+  return butterfly<FULL, NW>(q);
+}
+
+// FULL: the row's 16-byte vectors divide evenly over the CTA's threads.
+template <int DT, int THREADS, int NV, bool TMA, bool FULL>
 __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int stages) {
   using IO = Io<DT>;
   constexpr int VEC = IO::kVec;
@@ -50,12 +60,12 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
   const uint32_t slot = has_r ? 2u * rb : rb;
   const uint32_t data_bytes = TMA ? static_cast<uint32_t>(stages) * slot : 0u;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + data_bytes);
-  Stats* red = reinterpret_cast<Stats*>(smem + data_bytes + 16);  // [2][NW]
+  Part* red = reinterpret_cast<Part*>(smem + data_bytes + 16);  // [2][NW]
   const uint32_t smem0 = smem_addr(smem);
 
   bool ok[NV];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) ok[k] = (tid + THREADS * k) < nvec;
+  for (int k = 0; k < NV; ++k) ok[k] = FULL || (tid + THREADS * k) < nvec;
 
   const int64_t stride = gridDim.x;
   int64_t row = blockIdx.x;
@@ -95,6 +105,7 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
       for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
 
     bool timed_out = false;
+    float K;  // the row's shift: its first sum a_0
     if constexpr (TMA) {
       const int s = static_cast<int>(it % stages);
       const uint32_t parity = static_cast<uint32_t>((it / stages) & 1);
@@ -114,7 +125,19 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
           }
         }
       }
+      // a_0 from the staged copy (a broadcast read; unaffected by any global
+      // store, so A may alias R)
+      float t[VEC];
+      IO::unpack(ld_shared_v4(xs), t);
+      K = t[0];
+      if (has_r) {
+        IO::unpack(ld_shared_v4(xs + rb), t);
+        K += t[0];
+      }
     } else {
+      // a_0 from global memory, read before the barrier below; every global
+      // store of this row comes after that barrier, so in-place is safe
+      K = has_r ? IO::load1(p.x, base) + IO::load1(p.r, base) : IO::load1(p.x, base);
       const char* xrow = static_cast<const char*>(p.x) + base * S;
       uint4 xv[NV], rv[NV];
 #pragma unroll
@@ -140,10 +163,28 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
       }
     }
 
-    // ---- statistics: per-thread two-pass, warp butterfly, CTA merge
-    Stats st = thread_stats<NV, VEC>(v, ok);
-    st = warp_allreduce(st, lane);
-    Stats* rbuf = red + (it & 1) * NW;
+    // ---- TMA path: A = X + R rounded to the dtype, stored at once
+    if (TMA && p.a != nullptr && !timed_out) {
+      char* arow = static_cast<char*>(p.a) + base * S;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (ok[k]) st_stream_v4(arow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::pack(v[k]));
+    }
+
+    // ---- statistics: per-thread two-pass on the shifted row, warp
+    // butterfly, then the CTA merge of the warp partials
+    Part st;
+    if constexpr (TMA) {
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) v[k][e] -= K;
+      st = thread_part<NV, VEC, FULL>(v, ok, 0.f);
+    } else {
+      st = thread_part<NV, VEC, FULL>(v, ok, K);
+    }
+    st = butterfly<FULL, 32>(st);
+    Part* rbuf = red + (it & 1) * NW;
     if (lane == 0) rbuf[warp] = st;
 
     if constexpr (TMA) {
@@ -168,11 +209,10 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
       __syncthreads();
     }
 
-    Stats tot = {0.f, 0.f, 0.f};
-    if (lane < NW) tot = rbuf[lane];
-    tot = warp_allreduce(tot, lane);
-    const float mean = tot.m;
-    const float rstd = row_rstd(tot, H, p.eps);
+    const Part tot = cta_totals<FULL, NW>(rbuf, lane);
+    const float m = tot.m;
+    const float rstd = row_rstd(tot.M2, p.inv_h, p.eps);
+    const float Kn = TMA ? 0.f : K;  // shift still to remove before normalising
 
     // ---- normalise + affine from registers, store
     char* yrow = static_cast<char*>(p.y) + base * S;
@@ -185,22 +225,22 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
         for (int q = 0; q < VEC / 4; ++q) {
           const float4 g = ld_param_f4(p.gamma + c * VEC + 4 * q);
           const float4 b = ld_param_f4(p.beta + c * VEC + 4 * q);
-          o[4 * q + 0] = fmaf((v[k][4 * q + 0] - mean) * rstd, g.x, b.x);
-          o[4 * q + 1] = fmaf((v[k][4 * q + 1] - mean) * rstd, g.y, b.y);
-          o[4 * q + 2] = fmaf((v[k][4 * q + 2] - mean) * rstd, g.z, b.z);
-          o[4 * q + 3] = fmaf((v[k][4 * q + 3] - mean) * rstd, g.w, b.w);
+          o[4 * q + 0] = normalise(v[k][4 * q + 0], Kn, m, rstd, g.x, b.x);
+          o[4 * q + 1] = normalise(v[k][4 * q + 1], Kn, m, rstd, g.y, b.y);
+          o[4 * q + 2] = normalise(v[k][4 * q + 2], Kn, m, rstd, g.z, b.z);
+          o[4 * q + 3] = normalise(v[k][4 * q + 3], Kn, m, rstd, g.w, b.w);
         }
         st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::pack(o));
       }
     }
-    if (p.a != nullptr) {
+    if (!TMA && p.a != nullptr) {
       char* arow = static_cast<char*>(p.a) + base * S;
 #pragma unroll
       for (int k = 0; k < NV; ++k)
         if (ok[k]) st_stream_v4(arow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::pack(v[k]));
     }
     if (tid == 0) {
-      if (p.mean != nullptr) p.mean[row] = mean;
+      if (p.mean != nullptr) p.mean[row] = K + m;
       if (p.rstd != nullptr) p.rstd[row] = rstd;
     }
   }
@@ -209,7 +249,8 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
 // Element-wise variant: any alignment, any H up to the maximum.  Each thread
 // keeps the fp32 sums of its own elements (j = tid + THREADS*k) in shared
 // memory, so no thread reads another's slots and only the statistics need a
-// barrier.
+// barrier.  All global stores of a row follow that barrier, by which time
+// every thread has read a_0, so outputs may alias inputs.
 template <int DT, int THREADS>
 __global__ void __launch_bounds__(THREADS) k_cta_scalar(const RowArgs p) {
   using IO = Io<DT>;
@@ -217,13 +258,14 @@ __global__ void __launch_bounds__(THREADS) k_cta_scalar(const RowArgs p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int H = p.H;
   float* sa = reinterpret_cast<float*>(smem);
-  Stats* red = reinterpret_cast<Stats*>(smem + ((static_cast<uint32_t>(H) * 4u + 127u) & ~127u));
+  Part* red = reinterpret_cast<Part*>(smem + ((static_cast<uint32_t>(H) * 4u + 127u) & ~127u));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool has_r = p.r != nullptr;
 
   int64_t it = 0;
   for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
     const int64_t base = row * static_cast<int64_t>(H);
+    const float K = has_r ? IO::load1(p.x, base) + IO::load1(p.r, base) : IO::load1(p.x, base);
     float sum = 0.f;
     int cnt = 0;
 #pragma unroll 8
@@ -231,35 +273,32 @@ __global__ void __launch_bounds__(THREADS) k_cta_scalar(const RowArgs p) {
       float a = IO::load1(p.x, base + j);
       if (has_r) a += IO::load1(p.r, base + j);
       sa[j] = a;
-      sum += a;
+      sum += a - K;
       ++cnt;
     }
-    Stats st;
+    Part st;
     st.n = static_cast<float>(cnt);
     st.m = cnt ? __fdiv_rn(sum, st.n) : 0.f;
     float M2 = 0.f;
     for (int j = tid; j < H; j += THREADS) {
-      const float d = sa[j] - st.m;
+      const float d = (sa[j] - K) - st.m;
       M2 = fmaf(d, d, M2);
     }
     st.M2 = M2;
-    st = warp_allreduce(st, lane);
-    Stats* rbuf = red + (it & 1) * NW;
+    st = butterfly<false, 32>(st);
+    Part* rbuf = red + (it & 1) * NW;
     if (lane == 0) rbuf[warp] = st;
     __syncthreads();
-    Stats tot = {0.f, 0.f, 0.f};
-    if (lane < NW) tot = rbuf[lane];
-    tot = warp_allreduce(tot, lane);
-    const float mean = tot.m;
-    const float rstd = row_rstd(tot, H, p.eps);
+    const Part tot = cta_totals<false, NW>(rbuf, lane);
+    const float rstd = row_rstd(tot.M2, p.inv_h, p.eps);
 #pragma unroll 4
     for (int j = tid; j < H; j += THREADS) {
       const float a = sa[j];
-      IO::store1(p.y, base + j, fmaf((a - mean) * rstd, __ldg(p.gamma + j), __ldg(p.beta + j)));
+      IO::store1(p.y, base + j, normalise(a, K, tot.m, rstd, __ldg(p.gamma + j), __ldg(p.beta + j)));
       if (p.a != nullptr) IO::store1(p.a, base + j, a);
     }
     if (tid == 0) {
-      if (p.mean != nullptr) p.mean[row] = mean;
+      if (p.mean != nullptr) p.mean[row] = K + tot.m;
       if (p.rstd != nullptr) p.rstd[row] = rstd;
     }
   }
@@ -310,13 +349,13 @@ int64_t persistent_grid(int64_t rows, int per_sm, const LaunchCtx& c) {
   return g;
 }
 
-template <int DT, int THREADS, int NV, bool TMA>
-int launch_row(const RowArgs& p, const LaunchCtx& c) {
+template <int DT, int THREADS, int NV, bool TMA, bool FULL>
+int launch_row_t(const RowArgs& p, const LaunchCtx& c) {
   constexpr int S = Io<DT>::kBytes;
   const uint32_t row_bytes = static_cast<uint32_t>(p.H) * S;
   const uint32_t rb = (row_bytes + 127u) & ~127u;
   const uint32_t slot = p.r ? 2u * rb : rb;
-  const uint32_t extra = 16u + 2u * (THREADS / 32) * sizeof(Stats);
+  const uint32_t extra = 16u + 2u * (THREADS / 32) * sizeof(Part);
   int stages = 0;
   uint32_t smem = extra;
   if (TMA) {
@@ -324,14 +363,21 @@ int launch_row(const RowArgs& p, const LaunchCtx& c) {
     smem = stages * slot + extra;
     if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
   }
-  const void* f = reinterpret_cast<const void*>(&k_cta_row<DT, THREADS, NV, TMA>);
+  const void* f = reinterpret_cast<const void*>(&k_cta_row<DT, THREADS, NV, TMA, FULL>);
   const int per_sm = resident_ctas(f, THREADS, static_cast<int>(smem), c.dev);
   if (per_sm < 0) return ADDLN_ERR_CUDA;
   if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
   const int64_t grid = persistent_grid(p.rows, per_sm, c);
-  k_cta_row<DT, THREADS, NV, TMA>
+  k_cta_row<DT, THREADS, NV, TMA, FULL>
       <<<static_cast<unsigned>(grid), THREADS, smem, static_cast<cudaStream_t>(c.stream)>>>(p, stages);
   return cudaGetLastError() == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+}
+
+template <int DT, int THREADS, int NV, bool TMA>
+int launch_row(const RowArgs& p, const LaunchCtx& c) {
+  const bool full = p.H / Io<DT>::kVec == THREADS * NV;
+  return full ? launch_row_t<DT, THREADS, NV, TMA, true>(p, c)
+              : launch_row_t<DT, THREADS, NV, TMA, false>(p, c);
 }
 
 // (threads, vectors per thread) by the number of 16-byte vectors in a row.
@@ -355,7 +401,7 @@ template <int DT>
 int launch_scalar_impl(const RowArgs& p, const LaunchCtx& c) {
   constexpr int THREADS = 512;
   const uint32_t smem = ((static_cast<uint32_t>(p.H) * 4u + 127u) & ~127u) +
-                        2u * (THREADS / 32) * sizeof(Stats);
+                        2u * (THREADS / 32) * sizeof(Part);
   if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
   const void* f = reinterpret_cast<const void*>(&k_cta_scalar<DT, THREADS>);
   const int per_sm = resident_ctas(f, THREADS, static_cast<int>(smem), c.dev);

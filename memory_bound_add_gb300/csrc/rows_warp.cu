@@ -1,11 +1,14 @@
 // One warp per row: fused residual add + LayerNorm for short rows (H <= 1024).
 //
 // Each lane loads its share of the row of X and R with 16-byte streaming
-// loads (vector path) or element loads (scalar path, any alignment), adds
-// them in fp32 registers, takes two-pass statistics of its own values, and
-// the warp merges them with a butterfly of Chan updates.  The row never
-// leaves registers: X and R are read once, Y (and optionally A, mean, rstd)
-// written once -- the fused traffic of "算子融合的收益量化" section 1.
+// loads (vector path) or element loads (scalar path, any alignment) and adds
+// them in fp32 registers.  A (when requested) is stored straight away.  The
+// values are then shifted by the row's first sum a_0, which lane 0 holds and
+// broadcasts by shuffle; each lane takes two-pass statistics of its own
+// values and the warp merges them with a xor butterfly of Chan updates.  The
+// row never leaves registers: X and R are read once, Y (and optionally A,
+// mean, rstd) written once -- the fused traffic of "算子融合的收益量化"
+// section 1.
 #include "../../include/addln.h"
 #include "common.cuh"
 
@@ -14,8 +17,9 @@ namespace addln {
 constexpr int kWarpCtaThreads = 256;  // 8 rows per CTA
 constexpr int kRowsPerCta = kWarpCtaThreads / 32;
 
-template <int DT, int NV, bool VECTOR>
-__global__ void __launch_bounds__(kWarpCtaThreads) k_warp_row(const RowArgs p) {
+// FULL: the row's vectors (elements) divide evenly over the 32 lanes.
+template <int DT, int NV, bool VECTOR, bool FULL>
+__global__ void __launch_bounds__(kWarpCtaThreads, 2) k_warp_row(const RowArgs p) {
   using IO = Io<DT>;
   constexpr int VEC = VECTOR ? IO::kVec : 1;
   constexpr int S = IO::kBytes;
@@ -28,7 +32,7 @@ __global__ void __launch_bounds__(kWarpCtaThreads) k_warp_row(const RowArgs p) {
 
   bool ok[NV];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) ok[k] = (lane + 32 * k) < nvec;
+  for (int k = 0; k < NV; ++k) ok[k] = FULL || (lane + 32 * k) < nvec;
 
   float v[NV][VEC];
 #pragma unroll
@@ -76,11 +80,30 @@ __global__ void __launch_bounds__(kWarpCtaThreads) k_warp_row(const RowArgs p) {
     }
   }
 
-  // ---- row statistics: per-lane two-pass, warp Chan butterfly
-  Stats st = thread_stats<NV, VEC>(v, ok);
-  st = warp_allreduce(st, lane);
-  const float mean = st.m;
-  const float rstd = row_rstd(st, H, p.eps);
+  // ---- A = X + R rounded to the dtype; each lane writes only what it read
+  if (p.a != nullptr) {
+    if constexpr (VECTOR) {
+      char* arow = static_cast<char*>(p.a) + base * S;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (ok[k]) st_stream_v4(arow + static_cast<int64_t>(lane + 32 * k) * 16, IO::pack(v[k]));
+    } else {
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (ok[k]) IO::store1(p.a, base + lane + 32 * k, v[k][0]);
+    }
+  }
+
+  // ---- row statistics on the shifted row: per-lane two-pass, warp butterfly
+  const float K = __shfl_sync(0xffffffffu, v[0][0], 0);  // a_0, held by lane 0
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) v[k][e] -= K;
+  Part st = thread_part<NV, VEC, FULL>(v, ok, 0.f);
+  st = butterfly<FULL, 32>(st);
+  const float m = st.m;
+  const float rstd = row_rstd(st.M2, p.inv_h, p.eps);
 
   // ---- normalise + affine, store
   if constexpr (VECTOR) {
@@ -94,19 +117,13 @@ __global__ void __launch_bounds__(kWarpCtaThreads) k_warp_row(const RowArgs p) {
         for (int q = 0; q < VEC / 4; ++q) {
           const float4 g = ld_param_f4(p.gamma + c * VEC + 4 * q);
           const float4 b = ld_param_f4(p.beta + c * VEC + 4 * q);
-          o[4 * q + 0] = fmaf((v[k][4 * q + 0] - mean) * rstd, g.x, b.x);
-          o[4 * q + 1] = fmaf((v[k][4 * q + 1] - mean) * rstd, g.y, b.y);
-          o[4 * q + 2] = fmaf((v[k][4 * q + 2] - mean) * rstd, g.z, b.z);
-          o[4 * q + 3] = fmaf((v[k][4 * q + 3] - mean) * rstd, g.w, b.w);
+          o[4 * q + 0] = normalise(v[k][4 * q + 0], 0.f, m, rstd, g.x, b.x);
+          o[4 * q + 1] = normalise(v[k][4 * q + 1], 0.f, m, rstd, g.y, b.y);
+          o[4 * q + 2] = normalise(v[k][4 * q + 2], 0.f, m, rstd, g.z, b.z);
+          o[4 * q + 3] = normalise(v[k][4 * q + 3], 0.f, m, rstd, g.w, b.w);
         }
         st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::pack(o));
       }
-    }
-    if (p.a != nullptr) {
-      char* arow = static_cast<char*>(p.a) + base * S;
-#pragma unroll
-      for (int k = 0; k < NV; ++k)
-        if (ok[k]) st_stream_v4(arow + static_cast<int64_t>(lane + 32 * k) * 16, IO::pack(v[k]));
     }
   } else {
 #pragma unroll
@@ -114,17 +131,12 @@ __global__ void __launch_bounds__(kWarpCtaThreads) k_warp_row(const RowArgs p) {
       if (ok[k]) {
         const int j = lane + 32 * k;
         const float g = __ldg(p.gamma + j), b = __ldg(p.beta + j);
-        IO::store1(p.y, base + j, fmaf((v[k][0] - mean) * rstd, g, b));
+        IO::store1(p.y, base + j, normalise(v[k][0], 0.f, m, rstd, g, b));
       }
-    }
-    if (p.a != nullptr) {
-#pragma unroll
-      for (int k = 0; k < NV; ++k)
-        if (ok[k]) IO::store1(p.a, base + lane + 32 * k, v[k][0]);
     }
   }
   if (lane == 0) {
-    if (p.mean != nullptr) p.mean[row] = mean;
+    if (p.mean != nullptr) p.mean[row] = K + m;
     if (p.rstd != nullptr) p.rstd[row] = rstd;
   }
 }
@@ -133,8 +145,13 @@ template <int DT, int NV, bool VECTOR>
 static int launch(const RowArgs& p, const LaunchCtx& c) {
   const int64_t blocks = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
   if (blocks > 0x7fffffff) return ADDLN_ERR_UNSUPPORTED;
-  k_warp_row<DT, NV, VECTOR>
-      <<<static_cast<unsigned>(blocks), kWarpCtaThreads, 0, static_cast<cudaStream_t>(c.stream)>>>(p);
+  constexpr int VEC = VECTOR ? Io<DT>::kVec : 1;
+  const bool full = (p.H / VEC) == 32 * NV;
+  cudaStream_t s = static_cast<cudaStream_t>(c.stream);
+  if (full)
+    k_warp_row<DT, NV, VECTOR, true><<<static_cast<unsigned>(blocks), kWarpCtaThreads, 0, s>>>(p);
+  else
+    k_warp_row<DT, NV, VECTOR, false><<<static_cast<unsigned>(blocks), kWarpCtaThreads, 0, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
 
