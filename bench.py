@@ -67,6 +67,11 @@ def parse_args():
     ap.add_argument("--path", type=int, default=0, help="force a kernel path (ADDLN_PATH_*)")
     ap.add_argument("--grid-cap", type=int, default=0)
     ap.add_argument("--graph-steps", type=int, default=0, help="launches per captured graph")
+    ap.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch (1/0)")
+    ap.add_argument("--cta-threads", type=int, default=0, help="TMA kernel threads per CTA (tuning)")
+    ap.add_argument("--stages", type=int, default=0, help="TMA kernel staged rows per CTA (tuning)")
+    ap.add_argument("--kernel", choices=["fused", "add"], default="fused",
+                    help="add: time the unfused add kernel alone (same bytes as Y-only fused)")
     ap.add_argument("--only-fused", action="store_true",
                     help="time the fused kernel only (for profiling runs)")
     return ap.parse_args()
@@ -299,15 +304,20 @@ def run_ours(args):
 
     mba.addln_set_force_path(args.path)
     mba.addln_set_grid_cap(args.grid_cap)
+    mba.addln_set_pdl(args.pdl)
+    mba.addln_set_cta_shape(args.cta_threads, args.stages)
 
     def fused_step(i):
         s = sets[i]
+        if args.kernel == "add":
+            mba.add_fwd(s["x"], s["r"], s["y"])
+            return
         mba.add_layernorm_fwd(s["x"], s["r"], gamma, beta, s["y"], s["a"], s["mean"], s["rstd"],
                               eps=eps)
 
     fused_step(0)
     torch.cuda.synchronize()
-    path = mba.addln_last_path()
+    path = mba.addln_last_path() if args.kernel == "fused" else "add_vec"
     if mba.addln_get_device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
 
@@ -363,6 +373,7 @@ def run_ours(args):
                   f">= 3x the {l2 / 1e6:.0f} MB L2)",
             "graph": f"{graph_steps} launches per CUDA graph",
             "kernel_path": path,
+            "pdl": bool(args.pdl),
             "parallelism": f"{ws} independent replica(s), no collective on the data path",
         },
         "rows_per_s": round(ws * w.rows * K / elapsed, 1),
@@ -409,6 +420,7 @@ def run_ours(args):
         result["cpu_baseline"] = cpu_baseline(w, d, args.cpu_seconds)
     mba.addln_set_force_path(0)
     mba.addln_set_grid_cap(0)
+    mba.addln_set_cta_shape(0, 0)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws > 1:

@@ -140,11 +140,31 @@ int addln_set_force_path(int path);
 uint64_t addln_set_wait_limit_ns(uint64_t ns);
 
 /*
- * Test and benchmark only.  Caps the grid of the persistent CTA-per-row
- * kernels at `ctas` CTAs (0 = one wave of resident CTAs, the default).
- * Returns the previous cap.
+ * Test and benchmark only.  Sets the grid of the persistent CTA-per-row
+ * kernels to min(ctas, rows) CTAs, which may be more than one wave
+ * (0 = one wave of resident CTAs, the default).  Returns the previous value.
  */
 int64_t addln_set_grid_cap(int64_t ctas);
+
+/*
+ * Test and benchmark only.  Programmatic dependent launch (default 1 = on):
+ * every kernel is launched with programmatic stream serialisation, lets the
+ * next kernel in the stream begin launching once all its CTAs run, and waits
+ * for the previous kernel's completion before its first global memory
+ * access, so stream order and data dependences are kept.  0 launches plainly.
+ * Returns the previous setting.
+ */
+int addln_set_pdl(int on);
+
+/*
+ * Test and benchmark only.  Shape of the TMA CTA-per-row kernel: `threads`
+ * per CTA (64, 128, 256 or 512; 16-bit rows of at most 4096 elements; 0 =
+ * chosen from H) and `stages` rows staged per CTA (1..8; 0 = chosen from the
+ * shared memory size).  A shape that cannot run a call makes it return
+ * ADDLN_ERR_UNSUPPORTED.  Returns the previous thread setting, or
+ * ADDLN_ERR_SHAPE for a value out of range.
+ */
+int addln_set_cta_shape(int threads, int stages);
 
 /* Name of the kernel path the last add_layernorm_fwd / layernorm_fwd call on
  * this host thread launched (static text; "none" before the first launch). */

@@ -14,6 +14,8 @@ from .binding import (  # noqa: F401
     addln_set_force_path,
     addln_set_wait_limit_ns,
     addln_set_grid_cap,
+    addln_set_pdl,
+    addln_set_cta_shape,
     addln_last_path,
     addln_max_hidden,
     addln_strerror,

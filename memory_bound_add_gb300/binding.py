@@ -41,6 +41,8 @@ SIGNATURES = {
     "addln_set_force_path": (ctypes.c_int, [ctypes.c_int]),
     "addln_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "addln_set_grid_cap": (ctypes.c_int64, [ctypes.c_int64]),
+    "addln_set_pdl": (ctypes.c_int, [ctypes.c_int]),
+    "addln_set_cta_shape": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "addln_last_path": (ctypes.c_char_p, []),
 }
 
@@ -197,6 +199,14 @@ def addln_set_wait_limit_ns(ns: int) -> int:
 
 def addln_set_grid_cap(ctas: int) -> int:
     return int(lib().addln_set_grid_cap(int(ctas)))
+
+
+def addln_set_pdl(on: bool) -> int:
+    return int(lib().addln_set_pdl(int(bool(on))))
+
+
+def addln_set_cta_shape(threads: int, stages: int) -> int:
+    return int(lib().addln_set_cta_shape(int(threads), int(stages)))
 
 
 def addln_last_path() -> str:

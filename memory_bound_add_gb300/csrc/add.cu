@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(kAddThreads) k_add_vec(const void* x, const vo
   const uint4* xv = static_cast<const uint4*>(x);
   const uint4* rv = static_cast<const uint4*>(r);
   uint4* av = static_cast<uint4*>(a);
+  pdl_trigger();
+  pdl_wait();
   const int64_t step = static_cast<int64_t>(gridDim.x) * kAddThreads * kAddUnroll;
   for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kAddThreads * kAddUnroll + threadIdx.x;
        i0 < nvec; i0 += step) {
@@ -55,6 +57,8 @@ template <int DT>
 __global__ void __launch_bounds__(kAddThreads) k_add_scalar(const void* x, const void* r, void* a,
                                                             int64_t n) {
   using IO = Io<DT>;
+  pdl_trigger();
+  pdl_wait();
   const int64_t step = static_cast<int64_t>(gridDim.x) * kAddThreads;
   for (int64_t j = static_cast<int64_t>(blockIdx.x) * kAddThreads + threadIdx.x; j < n; j += step)
     IO::store1(a, j, IO::load1(x, j) + IO::load1(r, j));
@@ -65,19 +69,21 @@ static int launch_add_t(const void* x, const void* r, void* a, int64_t n, const 
   constexpr int VEC = Io<DT>::kVec;
   const int64_t max_blocks = static_cast<int64_t>(c.dev.sms) * (2048 / kAddThreads);
   auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
-  cudaStream_t s = static_cast<cudaStream_t>(c.stream);
+  cudaError_t e;
   if (al(x) && al(r) && al(a)) {
     const int64_t nvec = n / VEC;
     int64_t blocks = (nvec + kAddThreads * kAddUnroll - 1) / (kAddThreads * kAddUnroll);
     if (blocks > max_blocks) blocks = max_blocks;
     if (blocks < 1) blocks = 1;
-    k_add_vec<DT><<<static_cast<unsigned>(blocks), kAddThreads, 0, s>>>(x, r, a, nvec, n);
+    e = launch_kernel(k_add_vec<DT>, dim3(static_cast<unsigned>(blocks)), dim3(kAddThreads), 0,
+                      c.stream, c.pdl, x, r, a, nvec, n);
   } else {
     int64_t blocks = (n + kAddThreads - 1) / kAddThreads;
     if (blocks > max_blocks) blocks = max_blocks;
-    k_add_scalar<DT><<<static_cast<unsigned>(blocks), kAddThreads, 0, s>>>(x, r, a, n);
+    e = launch_kernel(k_add_scalar<DT>, dim3(static_cast<unsigned>(blocks)), dim3(kAddThreads), 0,
+                      c.stream, c.pdl, x, r, a, n);
   }
-  return cudaGetLastError() == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+  return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
 
 int launch_add(int dtype, const void* x, const void* r, void* a, int64_t n, const LaunchCtx& c) {

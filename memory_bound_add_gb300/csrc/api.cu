@@ -28,6 +28,9 @@ namespace {
 std::atomic<int> g_force_path{ADDLN_PATH_AUTO};
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
 std::atomic<int64_t> g_grid_cap{0};
+std::atomic<int> g_pdl{1};
+std::atomic<int> g_cta_threads{0};
+std::atomic<int> g_stages{0};
 thread_local const char* g_last_path = "none";
 
 constexpr int kMaxDevices = 64;
@@ -127,6 +130,9 @@ int run_rows(const RowArgs& p, int dtype, void* stream) {
   LaunchCtx c;
   c.stream = stream;
   c.grid_cap = g_grid_cap.load(std::memory_order_relaxed);
+  c.pdl = g_pdl.load(std::memory_order_relaxed) != 0;
+  c.cta_threads = g_cta_threads.load(std::memory_order_relaxed);
+  c.stages = g_stages.load(std::memory_order_relaxed);
   const int rc = device_info(&c.dev);
   if (rc != ADDLN_OK) return rc;
 
@@ -202,6 +208,9 @@ int add_fwd(const void* x, const void* r, void* a, int64_t n, int dtype, void* s
   LaunchCtx c;
   c.stream = stream;
   c.grid_cap = 0;
+  c.pdl = g_pdl.load(std::memory_order_relaxed) != 0;
+  c.cta_threads = 0;
+  c.stages = 0;
   const int rc = device_info(&c.dev);
   if (rc != ADDLN_OK) return rc;
   return addln::launch_add(dtype, x, r, a, n, c);
@@ -242,6 +251,17 @@ int addln_set_force_path(int path) {
 uint64_t addln_set_wait_limit_ns(uint64_t ns) { return g_wait_limit_ns.exchange(ns); }
 
 int64_t addln_set_grid_cap(int64_t ctas) { return g_grid_cap.exchange(ctas < 0 ? 0 : ctas); }
+
+int addln_set_pdl(int on) { return g_pdl.exchange(on != 0 ? 1 : 0); }
+
+int addln_set_cta_shape(int threads, int stages) {
+  if (threads != 0 && threads != 64 && threads != 128 && threads != 256 && threads != 512)
+    return ADDLN_ERR_SHAPE;
+  if (stages < 0 || stages > 8) return ADDLN_ERR_SHAPE;
+  const int prev = g_cta_threads.exchange(threads);
+  g_stages.exchange(stages);
+  return prev;
+}
 
 const char* addln_last_path(void) { return g_last_path; }
 

@@ -132,6 +132,34 @@ __device__ __forceinline__ float4 ld_param_f4(const float* p) {
   return __ldg(reinterpret_cast<const float4*>(p));
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Every kernel here lets the next kernel in the stream start launching as
+// soon as all of its CTAs are running, and waits for the previous kernel's
+// grid to complete (memory flushed) before its first global access, so a
+// dependent chain keeps its order while launch latency and CTA prologues
+// overlap the previous kernel's tail.  Both are no-ops without the launch
+// attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launches kernel<<<grid, block, smem, stream>>>(args...), with the
+// programmatic-stream-serialisation attribute when pdl is set.
+template <typename... KArgs, typename... Args>
+__host__ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                   void* stream, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------- shared memory
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

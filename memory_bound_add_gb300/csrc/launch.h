@@ -37,7 +37,10 @@ struct DeviceInfo {
 struct LaunchCtx {
   void* stream;  // cudaStream_t
   DeviceInfo dev;
-  int64_t grid_cap;  // 0 = one wave of resident CTAs
+  int64_t grid_cap;  // 0 = one wave of resident CTAs, else min(grid_cap, rows) CTAs
+  bool pdl;          // launch with programmatic stream serialisation
+  int cta_threads;   // CTA-per-row kernels: threads per CTA, 0 = by H
+  int stages;        // TMA path: rows staged per CTA, 0 = by shared memory
 };
 
 // Each launcher returns 0, or ADDLN_ERR_UNSUPPORTED when its kernel family

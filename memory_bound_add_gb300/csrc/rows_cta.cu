@@ -5,9 +5,9 @@
 //
 // TMA variant: thread 0 stages whole rows of X and R into shared memory with
 // one-dimensional bulk copies (cp.async.bulk, completion counted on an
-// mbarrier).  With two stages the copy of the CTA's next-but-one row is in
-// flight while the current row is reduced and normalised, so every SM keeps
-// row-sized requests outstanding against HBM.  Each thread moves its slice
+// mbarrier).  With two stages the copy of the CTA's next row is issued the
+// moment the current row lands, so it streams in while the current row is
+// reduced and normalised and every SM keeps row-sized requests outstanding.  Each thread moves its slice
 // from shared memory into registers once; the reduction and the normalisation
 // both run on those registers, and Y / A go straight to global memory with
 // 16-byte streaming stores.
@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
     __syncthreads();
     policy = policy_evict_first();
   }
+  pdl_trigger();
+  pdl_wait();  // the previous kernel's writes are visible from here on
 
   // Thread 0: stage row `rr` of X (and R) into stage `s`.
   auto issue = [&](int s, int64_t rr) {
@@ -90,10 +92,22 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
       bulk_g2s(smem0 + s * slot + rb, static_cast<const char*>(p.r) + off, row_bytes, bar, policy);
   };
 
+  // Copies run stages-1 rows ahead.  With two or more stages the next copy is
+  // issued as soon as the current row has landed (into the stage the
+  // previous row just vacated), so each CTA's transfer of row i+1 overlaps
+  // its reduction of row i without front-loading the whole grid's rows into
+  // the first microseconds; with one stage it is issued once the row is in
+  // registers.
+  const int ahead = stages > 1 ? stages - 1 : 0;
   if constexpr (TMA) {
-    if (tid == 0)
-      for (int s = 0; s < stages; ++s)
-        if (row + s * stride < p.rows) issue(s, row + s * stride);
+    if (tid == 0) {
+      if (stages == 1) {
+        if (row < p.rows) issue(0, row);
+      } else {
+        for (int s = 0; s < ahead; ++s)
+          if (row + s * stride < p.rows) issue(s, row + s * stride);
+      }
+    }
   }
 
   for (int64_t it = 0; row < p.rows; ++it, row += stride) {
@@ -105,11 +119,21 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
       for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
 
     bool timed_out = false;
+    bool issued_ahead = false;
     float K;  // the row's shift: its first sum a_0
     if constexpr (TMA) {
       const int s = static_cast<int>(it % stages);
       const uint32_t parity = static_cast<uint32_t>((it / stages) & 1);
       timed_out = !mbar_wait_bounded(smem_addr(&bars[s]), parity, p.wait_limit_ns);
+      if (ahead > 0 && tid == 0 && !timed_out) {
+        // stage (it + ahead) % stages last held row it-1, which every thread
+        // finished reading before the previous iteration's barrier
+        const int64_t next = row + ahead * stride;
+        if (next < p.rows) {
+          issue(static_cast<int>((it + ahead) % stages), next);
+          issued_ahead = true;
+        }
+      }
       const uint32_t xs = smem0 + s * slot;
 #pragma unroll
       for (int k = 0; k < NV; ++k)
@@ -191,8 +215,10 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
       // Also the point after which no thread reads stage s any more.
       if (__syncthreads_or(timed_out)) {
         if (tid == 0) {
+          // copies in flight: rows it .. it+ahead-1, plus it+ahead if issued
           atomicExch(&g_device_error, ADDLN_ERR_DEVICE_TIMEOUT);
-          for (int j = 0; j < stages; ++j) {
+          const int pending = ahead > 0 ? ahead + (issued_ahead ? 1 : 0) : 1;
+          for (int j = 0; j < pending; ++j) {
             const int64_t itj = it + j;
             if (row + j * stride < p.rows)
               mbar_wait_bounded(smem_addr(&bars[itj % stages]),
@@ -201,9 +227,9 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
         }
         return;
       }
-      if (tid == 0) {
-        const int64_t next = row + stages * stride;
-        if (next < p.rows) issue(static_cast<int>(it % stages), next);
+      if (ahead == 0 && tid == 0) {
+        const int64_t next = row + stride;
+        if (next < p.rows) issue(0, next);
       }
     } else {
       __syncthreads();
@@ -261,6 +287,8 @@ __global__ void __launch_bounds__(THREADS) k_cta_scalar(const RowArgs p) {
   Part* red = reinterpret_cast<Part*>(smem + ((static_cast<uint32_t>(H) * 4u + 127u) & ~127u));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool has_r = p.r != nullptr;
+  pdl_trigger();
+  pdl_wait();
 
   int64_t it = 0;
   for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
@@ -342,9 +370,12 @@ int resident_ctas(const void* f, int threads, int smem, const DeviceInfo& dev) {
   return n;
 }
 
+// One wave of resident CTAs by default; a set grid cap replaces it (and may
+// exceed one wave, e.g. one CTA per row).
 int64_t persistent_grid(int64_t rows, int per_sm, const LaunchCtx& c) {
   int64_t g = static_cast<int64_t>(per_sm) * c.dev.sms;
-  if (c.grid_cap > 0 && c.grid_cap < g) g = c.grid_cap;
+  if (c.grid_cap > 0) g = c.grid_cap;
+  if (g > 0x7fffffff) g = 0x7fffffff;
   if (rows < g) g = rows;
   return g;
 }
@@ -359,7 +390,8 @@ int launch_row_t(const RowArgs& p, const LaunchCtx& c) {
   int stages = 0;
   uint32_t smem = extra;
   if (TMA) {
-    stages = (2u * slot + extra <= static_cast<uint32_t>(c.dev.smem_optin) / 2u) ? 2 : 1;
+    stages = c.stages > 0 ? c.stages
+                          : (2u * slot + extra <= static_cast<uint32_t>(c.dev.smem_optin) / 2u) ? 2 : 1;
     smem = stages * slot + extra;
     if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
   }
@@ -368,9 +400,10 @@ int launch_row_t(const RowArgs& p, const LaunchCtx& c) {
   if (per_sm < 0) return ADDLN_ERR_CUDA;
   if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
   const int64_t grid = persistent_grid(p.rows, per_sm, c);
-  k_cta_row<DT, THREADS, NV, TMA, FULL>
-      <<<static_cast<unsigned>(grid), THREADS, smem, static_cast<cudaStream_t>(c.stream)>>>(p, stages);
-  return cudaGetLastError() == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+  const cudaError_t e = launch_kernel(k_cta_row<DT, THREADS, NV, TMA, FULL>,
+                                      dim3(static_cast<unsigned>(grid)), dim3(THREADS), smem,
+                                      c.stream, c.pdl, p, stages);
+  return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
 
 template <int DT, int THREADS, int NV, bool TMA>
@@ -385,6 +418,16 @@ template <int DT, bool TMA>
 int launch_row_dispatch(const RowArgs& p, const LaunchCtx& c, const char** name) {
   constexpr int VEC = Io<DT>::kVec;
   const int nvec = p.H / VEC;
+  if (c.cta_threads != 0) {
+    // Tuning shapes (TMA staging of 16-bit rows only); otherwise by H below.
+    if constexpr (TMA && VEC == 8) {
+      if (c.cta_threads == 64 && nvec <= 64 * 8) { *name = "cta_tma_t64_nv8"; return launch_row<DT, 64, 8, true>(p, c); }
+      if (c.cta_threads == 128 && nvec <= 128 * 4) { *name = "cta_tma_t128_nv4"; return launch_row<DT, 128, 4, true>(p, c); }
+      if (c.cta_threads == 256 && nvec <= 256 * 2) { *name = "cta_tma_t256_nv2"; return launch_row<DT, 256, 2, true>(p, c); }
+      if (c.cta_threads == 512 && nvec <= 512 * 1) { *name = "cta_tma_t512_nv1"; return launch_row<DT, 512, 1, true>(p, c); }
+    }
+    return ADDLN_ERR_UNSUPPORTED;
+  }
   if (nvec <= 128 * 2) { *name = TMA ? "cta_tma_t128_nv2" : "cta_vec_t128_nv2"; return launch_row<DT, 128, 2, TMA>(p, c); }
   if (nvec <= 128 * 4) { *name = TMA ? "cta_tma_t128_nv4" : "cta_vec_t128_nv4"; return launch_row<DT, 128, 4, TMA>(p, c); }
   if (nvec <= 256 * 4) { *name = TMA ? "cta_tma_t256_nv4" : "cta_vec_t256_nv4"; return launch_row<DT, 256, 4, TMA>(p, c); }
@@ -408,9 +451,9 @@ int launch_scalar_impl(const RowArgs& p, const LaunchCtx& c) {
   if (per_sm < 0) return ADDLN_ERR_CUDA;
   if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
   const int64_t grid = persistent_grid(p.rows, per_sm, c);
-  k_cta_scalar<DT, THREADS>
-      <<<static_cast<unsigned>(grid), THREADS, smem, static_cast<cudaStream_t>(c.stream)>>>(p);
-  return cudaGetLastError() == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+  const cudaError_t e = launch_kernel(k_cta_scalar<DT, THREADS>, dim3(static_cast<unsigned>(grid)),
+                                      dim3(THREADS), smem, c.stream, c.pdl, p);
+  return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
 
 }  // namespace

@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kWarpCtaThreads, 2) k_warp_row(const RowArgs p
   constexpr int S = IO::kBytes;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
+  pdl_trigger();
+  pdl_wait();
   if (row >= p.rows) return;  // whole warp leaves together
   const int H = p.H;
   const int nvec = H / VEC;
@@ -147,12 +149,11 @@ static int launch(const RowArgs& p, const LaunchCtx& c) {
   if (blocks > 0x7fffffff) return ADDLN_ERR_UNSUPPORTED;
   constexpr int VEC = VECTOR ? Io<DT>::kVec : 1;
   const bool full = (p.H / VEC) == 32 * NV;
-  cudaStream_t s = static_cast<cudaStream_t>(c.stream);
-  if (full)
-    k_warp_row<DT, NV, VECTOR, true><<<static_cast<unsigned>(blocks), kWarpCtaThreads, 0, s>>>(p);
-  else
-    k_warp_row<DT, NV, VECTOR, false><<<static_cast<unsigned>(blocks), kWarpCtaThreads, 0, s>>>(p);
-  return cudaGetLastError() == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+  const dim3 grid(static_cast<unsigned>(blocks));
+  const cudaError_t e =
+      full ? launch_kernel(k_warp_row<DT, NV, VECTOR, true>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p)
+           : launch_kernel(k_warp_row<DT, NV, VECTOR, false>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p);
+  return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
 
 // Per-lane slot counts instantiated; the dispatcher takes the smallest that

@@ -45,7 +45,7 @@ def test_header_declares_the_expected_entry_points():
     assert header_functions() == sorted([
         "add_layernorm_fwd", "add_fwd", "layernorm_fwd", "addln_strerror", "addln_max_hidden",
         "addln_get_device_error", "addln_set_force_path", "addln_set_wait_limit_ns",
-        "addln_set_grid_cap", "addln_last_path"])
+        "addln_set_grid_cap", "addln_set_pdl", "addln_set_cta_shape", "addln_last_path"])
 
 
 def test_library_exports_every_header_symbol(lib):
@@ -92,6 +92,12 @@ def test_force_path_setter(lib):
     assert lib.addln_set_wait_limit_ns(1000000000) == 5
     assert lib.addln_set_grid_cap(3) == 0
     assert lib.addln_set_grid_cap(0) == 3
+    assert lib.addln_set_pdl(0) == 1
+    assert lib.addln_set_pdl(1) == 0
+    assert lib.addln_set_cta_shape(256, 3) == 0
+    assert lib.addln_set_cta_shape(0, 0) == 256
+    assert lib.addln_set_cta_shape(100, 0) == b.ERR_SHAPE
+    assert lib.addln_set_cta_shape(0, 9) == b.ERR_SHAPE
 
 
 BASE = 0x7F0000000000   # fake, 16-byte aligned

@@ -339,3 +339,60 @@ def test_full_size_sampled_rows(name):
     assert torch.isfinite(out["y"]).all()
     for i in d["const_rows"]:
         assert torch.equal(out["y"][i], d["beta"].to(TD[w.dtype]))
+
+
+# ------------------------------------------- programmatic dependent launch
+@pytest.mark.parametrize("name", ["bert_base_4096x768_fp16", "pages_2048x4096_fp16",
+                                  "tail_4096x1001_bf16"])
+def test_dependent_chain_keeps_order_under_pdl(name):
+    # each step reads the previous step's Y as its X: a kernel that touched
+    # memory before the previous grid finished would change the result
+    w = synth.with_rows(synth.get(name), 256)
+    d = _dev(synth.make_inputs(w, seed=12))
+    steps = 24
+
+    def chain():
+        x = d["x"].clone()
+        ys = []
+        for _ in range(steps):
+            y = torch.empty_like(x)
+            mba.add_layernorm_fwd(x, d["r"], d["gamma"], d["beta"], y, eps=d["eps"])
+            ys.append(y)
+            x = y
+        return ys
+
+    results = {}
+    for pdl in (0, 1):
+        prev = mba.addln_set_pdl(pdl)
+        try:
+            eager = chain()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                graphed = chain()
+            g.replay()
+            torch.cuda.synchronize()
+        finally:
+            mba.addln_set_pdl(prev)
+        results[pdl] = (eager[-1].cpu(), graphed[-1].cpu())
+        assert torch.equal(eager[-1], graphed[-1]), f"pdl={pdl}: graph differs from eager"
+    assert torch.equal(results[0][0], results[1][0])
+    # and the first step is right
+    x0 = synth.make_inputs(w, seed=12)
+    out = run_fused(x0, 0, want_a=False, want_stats=False)
+    check(w, x0, out, f"{name} chain step 0")
+
+
+@pytest.mark.parametrize("threads", [64, 128, 256, 512])
+@pytest.mark.parametrize("stages", [1, 2, 3])
+def test_tma_tuning_shapes(threads, stages):
+    w = synth.with_rows(synth.get("pages_2048x4096_fp16"), 150)
+    d = synth.make_inputs(w, seed=13)
+    prev = mba.addln_set_cta_shape(threads, stages)
+    try:
+        for cap in (0, 7):
+            out = run_fused(d, 0, grid_cap=cap)
+            assert out["path"] == f"cta_tma_t{threads}_nv{4096 // 8 // threads}"
+            check(w, d, out, f"tma t{threads} s{stages} cap{cap}")
+    finally:
+        mba.addln_set_cta_shape(0, 0)
