@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--rows", type=int, default=0,
+                    help="run the workload with this many rows (small profiling cases)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="bound on the CPU oracle baseline's timed work")
     ap.add_argument("--e2e-steps", type=int, default=200)
@@ -294,6 +296,8 @@ def run_ours(args):
             dist.barrier()
 
     w = synth.get(args.config)
+    if args.rows:
+        w = synth.with_rows(w, args.rows)
     d = synth.make_inputs(w, seed=args.seed + rank)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     n_sets = max(2, math.ceil(3 * l2 / set_bytes(w)))

@@ -294,16 +294,23 @@ __device__ __forceinline__ Part butterfly(Part p) {
 template <int NV, int VEC, bool FULL>
 __device__ __forceinline__ Part thread_part(const float (&v)[NV][VEC], const bool (&ok)[NV],
                                             float K) {
-  float sum = 0.f;
+  // four independent partial sums shorten the dependent-add chain
+  constexpr int L = VEC >= 4 ? 4 : VEC;
+  float acc[L];
+#pragma unroll
+  for (int l = 0; l < L; ++l) acc[l] = 0.f;
   int cnt = 0;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     if (FULL || ok[k]) {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) sum += v[k][e] - K;
+      for (int e = 0; e < VEC; ++e) acc[e % L] += v[k][e] - K;
       cnt += VEC;
     }
   }
+  float sum = acc[0];
+#pragma unroll
+  for (int l = 1; l < L; ++l) sum += acc[l];
   Part p;
   p.n = static_cast<float>(cnt);
   constexpr int kN = NV * VEC;
@@ -311,17 +318,22 @@ __device__ __forceinline__ Part thread_part(const float (&v)[NV][VEC], const boo
     p.m = sum * (1.0f / kN);  // exact: a power of two
   else
     p.m = cnt ? __fdiv_rn(sum, p.n) : 0.f;
-  float M2 = 0.f;
+  float sq[L];
+#pragma unroll
+  for (int l = 0; l < L; ++l) sq[l] = 0.f;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     if (FULL || ok[k]) {
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         const float d = (v[k][e] - K) - p.m;
-        M2 = fmaf(d, d, M2);
+        sq[e % L] = fmaf(d, d, sq[e % L]);
       }
     }
   }
+  float M2 = sq[0];
+#pragma unroll
+  for (int l = 1; l < L; ++l) M2 += sq[l];
   p.M2 = M2;
   return p;
 }

@@ -390,8 +390,10 @@ int launch_row_t(const RowArgs& p, const LaunchCtx& c) {
   int stages = 0;
   uint32_t smem = extra;
   if (TMA) {
-    stages = c.stages > 0 ? c.stages
-                          : (2u * slot + extra <= static_cast<uint32_t>(c.dev.smem_optin) / 2u) ? 2 : 1;
+    // One staged row per CTA by default: the shared memory a second stage
+    // takes costs more resident CTAs (rows reduced in parallel) than its
+    // prefetch gains (measured on 2048x4096 fp16 and 32768x8192 bf16).
+    stages = c.stages > 0 ? c.stages : 1;
     smem = stages * slot + extra;
     if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
   }
@@ -432,10 +434,10 @@ int launch_row_dispatch(const RowArgs& p, const LaunchCtx& c, const char** name)
   if (nvec <= 128 * 4) { *name = TMA ? "cta_tma_t128_nv4" : "cta_vec_t128_nv4"; return launch_row<DT, 128, 4, TMA>(p, c); }
   if (nvec <= 256 * 4) { *name = TMA ? "cta_tma_t256_nv4" : "cta_vec_t256_nv4"; return launch_row<DT, 256, 4, TMA>(p, c); }
   if (nvec <= 512 * 4) { *name = TMA ? "cta_tma_t512_nv4" : "cta_vec_t512_nv4"; return launch_row<DT, 512, 4, TMA>(p, c); }
-  // 1024 threads cap registers at 64 a thread: only the shared-memory staged
-  // variant fits there without spilling.
+  // The longest rows: 512 threads with 8 vectors each (a 1024-thread CTA
+  // would cap registers at 64 a thread, too few to hold the row).
   if constexpr (TMA) {
-    if (nvec <= 1024 * 4) { *name = "cta_tma_t1024_nv4"; return launch_row<DT, 1024, 4, true>(p, c); }
+    if (nvec <= 512 * 8) { *name = "cta_tma_t512_nv8"; return launch_row<DT, 512, 8, true>(p, c); }
   }
   return ADDLN_ERR_UNSUPPORTED;
 }
