@@ -206,14 +206,17 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// Tests phase `parity`; if it is not complete the thread may be suspended
+// (not spinning, so it takes no issue slots) until the phase completes or
+// about suspend_ns nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(suspend_ns)
       : "memory");
   return ok != 0;
 }
@@ -229,9 +232,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // phase has completed.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns) {
+  constexpr uint32_t kSuspendNs = 20000;
   if (limit_ns == 0) return false;
+  if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait(bar, parity, kSuspendNs)) {
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
   return true;
