@@ -87,6 +87,29 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank float over all ranks (the value itself when not
+    running distributed).  The only collective bench.py issues besides
+    barriers: the timed work itself exchanges nothing between ranks."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world_size: int, bytes_per_step: int, steps: int, elapsed_s: float) -> float:
+    """Aggregate effective GB/s of all replicas: every rank processes its own
+    batch each step, and the job takes as long as its slowest rank."""
+    return world_size * bytes_per_step * steps / elapsed_s / 1e9
+
+
+def replica_seed(seed: int, rank: int) -> int:
+    """Each replica draws its own batch (weak scaling, independent inputs)."""
+    return seed + rank
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -298,7 +321,7 @@ def run_ours(args):
     w = synth.get(args.config)
     if args.rows:
         w = synth.with_rows(w, args.rows)
-    d = synth.make_inputs(w, seed=args.seed + rank)
+    d = synth.make_inputs(w, seed=replica_seed(args.seed, rank))
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     n_sets = max(2, math.ceil(3 * l2 / set_bytes(w)))
     sets = make_sets(w, d, n_sets, dev)
@@ -343,14 +366,11 @@ def run_ours(args):
     if sampler:
         time.sleep(0.25)
         sampler.stop()
-    if ws > 1:
-        tt = torch.tensor([elapsed], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed = float(tt.item())
+    elapsed = max_over_ranks(elapsed, dev)
     if mba.addln_get_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
 
-    value = ws * alg * K / elapsed / 1e9
+    value = whole_job_gbs(ws, alg, K, elapsed)
     per_launch_s = elapsed / K
     achieved = alg / per_launch_s / 1e9
     peak, peak_kind = measured_peak()
@@ -405,6 +425,7 @@ def run_ours(args):
             mba.layernorm_fwd(a, gamma, beta, s["y"], s["mean"], s["rstd"], eps=eps)
         Ku = min(K, 20000)
         el_u, _, _ = timed_graph_run(unfused_step, Ku, W, n_sets, graph_steps, barrier)
+        el_u = max_over_ranks(el_u, dev)
         result["unfused_baseline"] = {
             "value": round(ws * alg * Ku / el_u / 1e9, 2),
             "unit": "GB/s (fused algorithmic bytes / time)",
@@ -477,10 +498,10 @@ def run_e2e(mba, w, d, dev, steps, W, barrier, ws):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    el = e0.elapsed_time(e1) / 1e3
+    el = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
     h2d = (hx.numel() + hr.numel()) * hx.element_size() + 8 * w.H
     d2h = hy.numel() * hy.element_size() * (2 if w.want_resid else 1) + (8 * w.rows if w.want_stats else 0)
-    return {"value": round(ws * w.algorithmic_bytes() * steps / el / 1e9, 2), "unit": "GB/s",
+    return {"value": round(whole_job_gbs(ws, w.algorithmic_bytes(), steps, el), 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(el / steps * 1e3, 4),
             "note": "add_layernorm_fwd with pinned host buffers; H2D, kernel, D2H on one stream"}
