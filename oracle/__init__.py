@@ -16,5 +16,6 @@ from .oracle import (
     oracle_add,
     oracle_layernorm,
     oracle_add_layernorm,
+    oracle_softmax,
     load,
 )

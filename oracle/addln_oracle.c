@@ -28,6 +28,13 @@
  *     even), returned as a double;
  *   - Y, mean and rstd are returned unrounded in fp64.
  *
+ * Row softmax ("算子融合与Kernel合并" 4.3, fused_softmax), per row i of X:
+ *   max_i  = max_j x_ij
+ *   sum_i  = sum_j exp(x_ij - max_i)
+ *   Y_ij   = exp(x_ij - max_i) / sum_i
+ * in the page's order: a max pass, an exp-sum pass, a divide pass; fp64
+ * throughout, libm exp.
+ *
  * dtype codes: 0 = IEEE binary32, 1 = IEEE binary16, 2 = bfloat16.
  * Return value: 0 on success, -1 on a bad argument.
  *
@@ -210,6 +217,45 @@ int oracle_add_layernorm(const void *x, const void *r, int dtype, const float *g
         if (a_out)
             for (int64_t j = 0; j < H; ++j)
                 a_out[i * H + j] = round_to_dtype(row[j], dtype);
+    }
+    free(row);
+    return 0;
+}
+
+/* Softmax of one row of H decoded values, in the page's three passes. */
+static void softmax_row(const double *x, int64_t H, double *y, double *max_out, double *sum_out)
+{
+    double mx = -INFINITY;
+    for (int64_t j = 0; j < H; ++j)
+        if (x[j] > mx)
+            mx = x[j];
+    double sum = 0.0;
+    for (int64_t j = 0; j < H; ++j)
+        sum += exp(x[j] - mx);
+    for (int64_t j = 0; j < H; ++j)
+        y[j] = exp(x[j] - mx) / sum;
+    if (max_out)
+        *max_out = mx;
+    if (sum_out)
+        *sum_out = sum;
+}
+
+/* Row softmax of X ([rows, H] in dtype); y receives fp64 [rows, H];
+ * row_max / row_sum (optional) receive max_i and sum_i. */
+int oracle_softmax(const void *x, int dtype, int64_t rows, int64_t H, double *y,
+                   double *row_max, double *row_sum)
+{
+    if (bad_dtype(dtype) || rows < 0 || H <= 0 || (rows > 0 && (!x || !y)))
+        return -1;
+    double *row = (double *)malloc((size_t)H * sizeof(double));
+    if (!row)
+        return -1;
+    const size_t esz = dtype == ORACLE_F32 ? 4 : 2;
+    for (int64_t i = 0; i < rows; ++i) {
+        const char *xi = (const char *)x + (size_t)(i * H) * esz;
+        for (int64_t j = 0; j < H; ++j)
+            row[j] = decode_at(xi, dtype, j);
+        softmax_row(row, H, y + i * H, row_max ? row_max + i : NULL, row_sum ? row_sum + i : NULL);
     }
     free(row);
     return 0;

@@ -34,8 +34,9 @@ def load():
             lib.oracle_layernorm.argtypes = [_P, _P, _P, _I64, _I64, ctypes.c_double, _P, _P, _P]
             lib.oracle_add_layernorm.argtypes = [_P, _P, ctypes.c_int, _P, _P, _I64, _I64,
                                                  ctypes.c_double, ctypes.c_int, _P, _P, _P, _P]
+            lib.oracle_softmax.argtypes = [_P, ctypes.c_int, _I64, _I64, _P, _P, _P]
             for f in ("oracle_decode", "oracle_round", "oracle_add", "oracle_layernorm",
-                      "oracle_add_layernorm"):
+                      "oracle_add_layernorm", "oracle_softmax"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -128,3 +129,17 @@ def oracle_add_layernorm(x, r, gamma, beta, eps: float, dtype: str, round_A: boo
                                        float(eps), int(round_A), _ptr(y), _ptr(a), _ptr(mean),
                                        _ptr(rstd)), "oracle_add_layernorm")
     return {"y": y, "a": a, "mean": mean, "rstd": rstd}
+
+
+def oracle_softmax(x, dtype: str) -> dict:
+    """Row softmax of host rows ``x`` ([rows, H] in dtype): fp64 y, and the
+    per-row max and exp-sum ("算子融合与Kernel合并" 4.3, fused_softmax)."""
+    xs = _raw(x, dtype)
+    assert xs.ndim == 2
+    rows, H = xs.shape
+    y = np.empty((rows, H), dtype=np.float64)
+    mx = np.empty(rows, dtype=np.float64)
+    sm = np.empty(rows, dtype=np.float64)
+    _check(load().oracle_softmax(_ptr(xs), _DT[dtype], rows, H, _ptr(y), _ptr(mx), _ptr(sm)),
+           "oracle_softmax")
+    return {"y": y, "max": mx, "sum": sm}

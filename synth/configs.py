@@ -42,6 +42,7 @@ class Workload:
     outlier_mag: float = 50.0
     note: str = ""
     shape_bsh: tuple = field(default=None)
+    op: str = "add_layernorm"     # or "softmax" (row softmax of X; R, gamma, beta unused)
 
     @property
     def n_const_rows(self) -> int:
@@ -58,12 +59,16 @@ class Workload:
     def algorithmic_bytes(self) -> int:
         """Minimal HBM bytes of one fused call over the whole batch.
 
+        Softmax: read X once, write Y once.
+
         Read X and R once, write Y once (plus A when requested), 8 bytes of
         fp32 statistics per row when requested, and gamma/beta (fp32 [H]) once.
         This is the fused-kernel accounting of "算子融合的收益量化" section 1
         extended by the optional outputs and the affine parameters.
         """
         s = self.elem_bytes
+        if self.op == "softmax":
+            return 2 * self.rows * self.H * s
         per_row = 2 * self.H * s + self.H * s * (1 + int(self.want_resid)) + 8 * int(self.want_stats)
         return self.rows * per_row + 8 * self.H
 
@@ -109,6 +114,21 @@ WORKLOADS = {
                  want_resid=True, want_stats=True, note="H not a multiple of 4 fp32"),
     ]
 }
+
+# Row softmax ("算子融合与Kernel合并" 4.3): the same reduce-elementwise pattern
+# on one input.  The pages give no sizes; these stand in for attention scores
+# (32 heads x 1024 queries over 1024 keys) and language-model logits over a
+# 32000-entry vocabulary, plus a small ragged fp32 case.
+SOFTMAX = [
+    Workload("softmax_tiny_64x1000_fp32", 64, 1000, "fp32", 0.0, x_dist=(0.0, 3.0), op="softmax",
+             note="small fp32 case, H not a multiple of 32 vectors"),
+    Workload("softmax_attention_32768x1024_fp16", 32768, 1024, "fp16", 0.0, x_dist=(0.0, 2.0),
+             op="softmax", note="attention scores, 32 heads x 1024 queries x 1024 keys"),
+    Workload("softmax_vocab_4096x32000_bf16", 4096, 32000, "bf16", 0.0, x_dist=(0.0, 4.0),
+             op="softmax", note="logits of 4096 tokens over a 32000-entry vocabulary"),
+]
+WORKLOADS.update({w.name: w for w in SOFTMAX})
+SOFTMAX_NAMES = [w.name for w in SOFTMAX]
 
 # The five workloads of the method's scope, in order; the rest are extra tails.
 PRIMARY = [

@@ -15,6 +15,7 @@ Recipe (every workload, in this fixed order of child streams of
      gets X_row = c (one N(x_loc, x_scale) draw) and R_row = 0
   5. outliers: round(frac * rows * H) positions of X chosen without
      replacement, each set to +-mag with a fair random sign
+(Softmax workloads draw no R: its stream is spawned but left unused.)
 X and R are then rounded to the I/O dtype with round-to-nearest-even (torch's
 float -> half / bfloat16 conversion).  Outputs are host (CPU) torch tensors.
 """
@@ -50,7 +51,7 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     n = rows * H
 
     x = _normal_f32(gx, n, *w.x_dist)
-    r = _normal_f32(gr, n, *w.r_dist)
+    r = _normal_f32(gr, n, *w.r_dist) if w.op != "softmax" else None
     gamma = (np.float32(1.0) + np.float32(0.1) * gg.standard_normal(H, dtype=np.float32)).astype(np.float32)
     beta = (np.float32(0.1) * gb.standard_normal(H, dtype=np.float32)).astype(np.float32)
 
@@ -71,10 +72,10 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
 
     td = TORCH_DTYPES[w.dtype]
     xt = torch.from_numpy(x).view(rows, H).to(td)
-    rt = torch.from_numpy(r).view(rows, H).to(td)
+    rt = torch.from_numpy(r).view(rows, H).to(td).contiguous() if r is not None else None
     return {
         "x": xt.contiguous(),
-        "r": rt.contiguous(),
+        "r": rt,
         "gamma": torch.from_numpy(gamma),
         "beta": torch.from_numpy(beta),
         "eps": float(w.eps),
