@@ -44,6 +44,7 @@ import torch  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "fused Add+LayerNorm effective HBM GB/s and % of GB300 peak; rows/sec"
+METRIC_SOFTMAX = "fused row softmax effective HBM GB/s and % of GB300 peak; rows/sec"
 DEFAULT_WORKLOAD = "pages_2048x4096_fp16"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
@@ -241,7 +242,7 @@ def make_sets(w, d, n_sets, dev):
     for _ in range(n_sets):
         s = {
             "x": d["x"].to(dev),
-            "r": d["r"].to(dev),
+            "r": d["r"].to(dev) if d["r"] is not None else None,
             "y": torch.empty(rows, w.H, dtype=d["x"].dtype, device=dev),
             "a": torch.empty(rows, w.H, dtype=d["x"].dtype, device=dev) if w.want_resid else None,
             "mean": torch.empty(rows, dtype=torch.float32, device=dev) if w.want_stats else None,
@@ -253,6 +254,8 @@ def make_sets(w, d, n_sets, dev):
 
 def set_bytes(w):
     s = w.elem_bytes
+    if w.op == "softmax":
+        return 2 * w.rows * w.H * s
     b = 3 * w.rows * w.H * s
     if w.want_resid:
         b += w.rows * w.H * s
@@ -339,6 +342,9 @@ def run_ours(args):
         if args.kernel == "add":
             mba.add_fwd(s["x"], s["r"], s["y"])
             return
+        if w.op == "softmax":
+            mba.softmax_fwd(s["x"], s["y"])
+            return
         mba.add_layernorm_fwd(s["x"], s["r"], gamma, beta, s["y"], s["a"], s["mean"], s["rstd"],
                               eps=eps)
 
@@ -375,7 +381,7 @@ def run_ours(args):
     achieved = alg / per_launch_s / 1e9
     peak, peak_kind = measured_peak()
     result = {
-        "metric": METRIC,
+        "metric": METRIC if w.op != "softmax" else METRIC_SOFTMAX,
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": ws,
@@ -390,8 +396,9 @@ def run_ours(args):
         "config": {
             "workload": w.name,
             "rows": w.rows, "H": w.H, "io_dtype": w.dtype,
+            "op": w.op,
             "outputs": "Y" + (", A" if w.want_resid else "") + (", mean, rstd" if w.want_stats else ""),
-            "eps": w.eps,
+            "eps": w.eps if w.op != "softmax" else None,
             "algorithmic_bytes_per_step": alg,
             "l2": f"inputs rotate over {n_sets} buffer sets ({n_sets * set_bytes(w) / 1e6:.0f} MB, "
                   f">= 3x the {l2 / 1e6:.0f} MB L2)",
@@ -417,7 +424,7 @@ def run_ours(args):
         },
     }
 
-    if not args.only_fused and not args.no_unfused:
+    if not args.only_fused and not args.no_unfused and w.op != "softmax":
         def unfused_step(i):
             s = sets[i]
             a = s["a"] if s["a"] is not None else s["y"]
@@ -456,14 +463,16 @@ def run_e2e(mba, w, d, dev, steps, W, barrier, ws):
     """Public API with host buffers: every step copies X, R, gamma, beta from
     pinned host memory, runs the fused call, and reads the outputs back into
     pinned host memory."""
-    hx, hr = d["x"].pin_memory(), d["r"].pin_memory()
+    soft = w.op == "softmax"
+    hx = d["x"].pin_memory()
+    hr = d["r"].pin_memory() if not soft else None
     hg, hb = d["gamma"].pin_memory(), d["beta"].pin_memory()
     hy = torch.empty_like(hx).pin_memory()
     ha = torch.empty_like(hx).pin_memory() if w.want_resid else None
     hm = torch.empty(w.rows, dtype=torch.float32).pin_memory() if w.want_stats else None
     hs = torch.empty(w.rows, dtype=torch.float32).pin_memory() if w.want_stats else None
     x = torch.empty_like(hx, device=dev)
-    r = torch.empty_like(hr, device=dev)
+    r = torch.empty_like(hr, device=dev) if not soft else None
     g = torch.empty_like(hg, device=dev)
     b = torch.empty_like(hb, device=dev)
     y = torch.empty_like(x)
@@ -473,6 +482,10 @@ def run_e2e(mba, w, d, dev, steps, W, barrier, ws):
 
     def step():
         x.copy_(hx, non_blocking=True)
+        if soft:
+            mba.softmax_fwd(x, y)
+            hy.copy_(y, non_blocking=True)
+            return
         r.copy_(hr, non_blocking=True)
         g.copy_(hg, non_blocking=True)
         b.copy_(hb, non_blocking=True)
@@ -499,7 +512,8 @@ def run_e2e(mba, w, d, dev, steps, W, barrier, ws):
     torch.cuda.synchronize()
     barrier()
     el = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
-    h2d = (hx.numel() + hr.numel()) * hx.element_size() + 8 * w.H
+    h2d = hx.numel() * hx.element_size() if soft else \
+        (hx.numel() + hr.numel()) * hx.element_size() + 8 * w.H
     d2h = hy.numel() * hy.element_size() * (2 if w.want_resid else 1) + (8 * w.rows if w.want_stats else 0)
     return {"value": round(whole_job_gbs(ws, w.algorithmic_bytes(), steps, el), 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
@@ -534,6 +548,8 @@ def cpu_model():
 
 def oracle_rows_call(w, d, lo, hi):
     import oracle
+    if w.op == "softmax":
+        return oracle.oracle_softmax(d["x"][lo:hi], w.dtype)
     return oracle.oracle_add_layernorm(d["x"][lo:hi], d["r"][lo:hi], d["gamma"], d["beta"],
                                        d["eps"], w.dtype, want_a=w.want_resid,
                                        want_stats=w.want_stats)
@@ -591,7 +607,7 @@ def run_reference(args):
     value = done * per_row / el / 1e9
     sample = f"{rows_per_step} rows of {w.name} per step, single-threaded fp64 C oracle"
     print(json.dumps({
-        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws, "steps": K,
+        "metric": METRIC if w.op != "softmax" else METRIC_SOFTMAX, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws, "steps": K,
         "warmup": W, "ms_per_step": round(el / K * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",

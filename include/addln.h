@@ -105,6 +105,18 @@ int add_fwd(const void *x, const void *r, void *a, int64_t n, int dtype, void *s
 int layernorm_fwd(const void *a, const float *gamma, const float *beta, void *y, float *mean,
                   float *rstd, int64_t rows, int64_t H, float eps, int dtype, void *stream);
 
+/*
+ * Fused row softmax ("算子融合与Kernel合并" 4.3, fused_softmax: a max reduce,
+ * an exp-sum reduce and a divide, here in one pass over the row):
+ *     Y_ij = exp(X_ij - max_j X_ij) / sum_k exp(X_ik - max_j X_ij)
+ *   x  [rows, H] input in dtype (required)
+ *   y  [rows, H] output in dtype (required); may be x exactly (in place)
+ * Arithmetic in fp32 with the hardware exponential (CUDA's __expf): relative
+ * error below 1e-5 wherever the result exceeds 1e-30; Y rounded to nearest
+ * even.  Same conventions and error codes as add_layernorm_fwd.
+ */
+int softmax_fwd(const void *x, void *y, int64_t rows, int64_t H, int dtype, void *stream);
+
 /* Static text for a return code (never NULL). */
 const char *addln_strerror(int code);
 
@@ -114,7 +126,8 @@ int64_t addln_max_hidden(int dtype);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error
- * word, which a kernel sets when a bounded wait on its own TMA copy runs out.
+ * words, which a kernel (add-LayerNorm or softmax) sets when a bounded wait
+ * on its own TMA copy runs out.
  * Returns ADDLN_OK, ADDLN_ERR_DEVICE_TIMEOUT, or ADDLN_ERR_CUDA if the
  * synchronisation or the read failed.  Rows of a kernel that timed out are
  * left unwritten.
@@ -122,8 +135,9 @@ int64_t addln_max_hidden(int dtype);
 int addln_get_device_error(void *stream);
 
 /*
- * Test and benchmark only.  Forces the kernel path of add_layernorm_fwd and
- * layernorm_fwd (ADDLN_PATH_*); ADDLN_PATH_AUTO restores the dispatcher.  A
+ * Test and benchmark only.  Forces the kernel path of add_layernorm_fwd,
+ * layernorm_fwd and softmax_fwd (ADDLN_PATH_*; softmax has no CTA_VEC path);
+ * ADDLN_PATH_AUTO restores the dispatcher.  A
  * forced path that cannot run a call's arguments makes that call return
  * ADDLN_ERR_UNSUPPORTED.  Returns the previous setting, or ADDLN_ERR_SHAPE
  * for an unknown path.

@@ -10,6 +10,8 @@ from .binding import (  # noqa: F401
     layernorm_fwd,
     add_layernorm,
     add_then_layernorm,
+    softmax_fwd,
+    softmax,
     addln_get_device_error,
     addln_set_force_path,
     addln_set_wait_limit_ns,

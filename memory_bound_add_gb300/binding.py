@@ -35,6 +35,7 @@ SIGNATURES = {
     "add_fwd": (ctypes.c_int, [_P, _P, _P, _I64, ctypes.c_int, _P]),
     "layernorm_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_float,
                                      ctypes.c_int, _P]),
+    "softmax_fwd": (ctypes.c_int, [_P, _P, _I64, _I64, ctypes.c_int, _P]),
     "addln_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "addln_max_hidden": (ctypes.c_int64, [ctypes.c_int]),
     "addln_get_device_error": (ctypes.c_int, [_P]),
@@ -179,6 +180,26 @@ def add_fwd(x, r, a, stream=None, n=None, dtype=None):
         n = x.numel() if n is None else n
         dtype = DTYPE_CODE[x.dtype] if dtype is None else dtype
     _check(lib().add_fwd(_ptr(x), _ptr(r), _ptr(a), int(n), int(dtype), _stream(stream)), "add_fwd")
+
+
+def softmax_fwd(x, y, stream=None, rows=None, H=None, dtype=None):
+    """Row softmax of x ([..., H]) into y."""
+    if isinstance(x, torch.Tensor):
+        rows_, H_ = _rows_shape(x)
+        _require(x, "x")
+        _require(y, "y", x.dtype, like=x)
+        rows = rows_ if rows is None else rows
+        H = H_ if H is None else H
+        dtype = DTYPE_CODE[x.dtype] if dtype is None else dtype
+    _check(lib().softmax_fwd(_ptr(x), _ptr(y), int(rows), int(H), int(dtype), _stream(stream)),
+           "softmax_fwd")
+
+
+def softmax(x, stream=None):
+    """Allocate y with PyTorch and run softmax_fwd."""
+    y = torch.empty_like(x)
+    softmax_fwd(x, y, stream=stream)
+    return y
 
 
 def addln_max_hidden(dtype: int) -> int:

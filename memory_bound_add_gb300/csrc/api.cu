@@ -170,9 +170,62 @@ int run_rows(const RowArgs& p, int dtype, void* stream) {
   return out;
 }
 
+int run_softmax(const RowArgs& p, int dtype, void* stream) {
+  LaunchCtx c;
+  c.stream = stream;
+  c.grid_cap = g_grid_cap.load(std::memory_order_relaxed);
+  c.pdl = g_pdl.load(std::memory_order_relaxed) != 0;
+  c.cta_threads = 0;
+  c.stages = 0;
+  const int rc = device_info(&c.dev);
+  if (rc != ADDLN_OK) return rc;
+  const int64_t row_bytes = static_cast<int64_t>(p.H) * elem_bytes(dtype);
+  const bool vec_ok = row_bytes % 16 == 0 && aligned16(p.x) && aligned16(p.y);
+  int path = g_force_path.load(std::memory_order_relaxed);
+  if (path == ADDLN_PATH_AUTO) {
+    if (p.H <= 1024)
+      path = vec_ok ? ADDLN_PATH_WARP_VEC : ADDLN_PATH_SCALAR;
+    else
+      path = vec_ok ? ADDLN_PATH_CTA_TMA : ADDLN_PATH_SCALAR;
+  }
+  const char* name = "none";
+  int out;
+  switch (path) {
+    case ADDLN_PATH_WARP_VEC:
+      if (!vec_ok || p.H > 1024) return ADDLN_ERR_UNSUPPORTED;
+      out = addln::launch_softmax_warp(dtype, true, p, c, &name);
+      break;
+    case ADDLN_PATH_CTA_TMA:
+      if (!vec_ok) return ADDLN_ERR_UNSUPPORTED;
+      out = addln::launch_softmax_cta(dtype, p, c, &name);
+      break;
+    case ADDLN_PATH_SCALAR:
+      out = p.H <= 1024 ? addln::launch_softmax_warp(dtype, false, p, c, &name)
+                        : addln::launch_softmax_scalar(dtype, p, c, &name);
+      break;
+    default:
+      return ADDLN_ERR_UNSUPPORTED;
+  }
+  if (out == ADDLN_OK) g_last_path = name;
+  return out;
+}
+
 }  // namespace
 
 extern "C" {
+
+int softmax_fwd(const void* x, void* y, int64_t rows, int64_t H, int dtype, void* stream) {
+  if (!valid_dtype(dtype)) return ADDLN_ERR_DTYPE;
+  if (rows < 0 || H <= 0 || H > max_hidden(dtype)) return ADDLN_ERR_SHAPE;
+  if (rows > INT64_MAX / (H * 4)) return ADDLN_ERR_SHAPE;
+  if (rows == 0) return ADDLN_OK;
+  if (!x || !y) return ADDLN_ERR_NULL;
+  const int64_t tb = rows * H * elem_bytes(dtype);
+  if (bad_pair(range_of(y, tb), range_of(x, tb), true)) return ADDLN_ERR_ALIAS;
+  RowArgs p{x, nullptr, nullptr, nullptr, y, nullptr, nullptr, nullptr, rows,
+            static_cast<int>(H), 0.f, 0.f, g_wait_limit_ns.load(std::memory_order_relaxed)};
+  return run_softmax(p, dtype, stream);
+}
 
 int add_layernorm_fwd(const void* x, const void* r, const float* gamma, const float* beta, void* y,
                       void* resid_out, float* mean, float* rstd, int64_t rows, int64_t H,
@@ -237,10 +290,12 @@ int64_t addln_max_hidden(int dtype) {
 }
 
 int addln_get_device_error(void* stream) {
-  int code = 0;
-  const int rc = addln::read_and_clear_device_error(stream, &code);
+  int code = 0, code_sm = 0;
+  int rc = addln::read_and_clear_device_error(stream, &code);
   if (rc != ADDLN_OK) return rc;
-  return code;
+  rc = addln::read_and_clear_softmax_error(&code_sm);
+  if (rc != ADDLN_OK) return rc;
+  return code != 0 ? code : code_sm;
 }
 
 int addln_set_force_path(int path) {

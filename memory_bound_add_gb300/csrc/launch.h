@@ -63,6 +63,14 @@ int launch_cta_scalar(int dtype, const RowArgs& p, const LaunchCtx& c, const cha
 // A = X + R over n elements.
 int launch_add(int dtype, const void* x, const void* r, void* a, int64_t n, const LaunchCtx& c);
 
+// Row softmax: one warp per row (vec: 16-byte loads), one CTA per row with
+// TMA staging, or one CTA per row with element loads.
+int launch_softmax_warp(int dtype, bool vec, const RowArgs& p, const LaunchCtx& c,
+                        const char** path_name);
+int launch_softmax_cta(int dtype, const RowArgs& p, const LaunchCtx& c, const char** path_name);
+int launch_softmax_scalar(int dtype, const RowArgs& p, const LaunchCtx& c, const char** path_name);
+int read_and_clear_softmax_error(int* code);
+
 // Device error word (set by a kernel whose bounded wait ran out).
 int read_and_clear_device_error(void* stream, int* code);
 

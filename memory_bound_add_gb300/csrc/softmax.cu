@@ -1,0 +1,444 @@
+// Fused row softmax: y_j = exp(x_j - max) / sum_k exp(x_k - max), the
+// reduce-elementwise pattern of fused_softmax in "算子融合与Kernel合并" 4.3
+// (max reduce, exp-sum reduce, divide), with the three passes fused into one
+// read of the row and one write.
+//
+// Each thread keeps its slice of the row in fp32 registers, takes its own
+// maximum m_t and replaces every value by e_j = exp(x_j - m_t) (one
+// exponential per element), summing s_t = sum e_j.  Partials (m, s) merge
+// with the online-softmax update
+//     m = max(m_a, m_b),  s = s_a * exp(m_a - m) + s_b * exp(m_b - m),
+// whose two terms are computed the same way on either side, so the xor
+// butterfly leaves identical totals (M, S) in every lane.  The output is
+// y_j = e_j * (exp(m_t - M) / S).  exp is CUDA's __expf (hardware base-2
+// exponential); its error grows with |x - max| but stays below 1e-5 relative
+// wherever the result is above 1e-30.
+//
+// Kernels: one warp per row for H <= 1024 (16-byte vector or element loads);
+// one CTA per row for longer rows, the row staged into shared memory by a TMA
+// bulk copy on a bounded mbarrier wait (persistent grid, one row staged per
+// CTA), or element loads into shared memory when rows are not 16-byte
+// aligned.
+#include <math.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/addln.h"
+#include "common.cuh"
+
+namespace addln {
+
+namespace sm {
+
+__device__ int g_softmax_error = 0;
+
+struct SPart {
+  float m;  // maximum of the covered values (-inf when none)
+  float s;  // sum of exp(value - m)
+};
+
+// Factor exp(from - to) with to >= from; exactly 1 when equal (which also
+// covers two empty partials, both -inf).
+__device__ __forceinline__ float rescale(float from, float to) {
+  return from == to ? 1.0f : __expf(from - to);
+}
+
+__device__ __forceinline__ SPart merge(const SPart& a, const SPart& b) {
+  SPart o;
+  o.m = fmaxf(a.m, b.m);
+  o.s = a.s * rescale(a.m, o.m) + b.s * rescale(b.m, o.m);
+  return o;
+}
+
+template <int WIDTH>
+__device__ __forceinline__ SPart butterfly(SPart p) {
+#pragma unroll
+  for (int off = 1; off < WIDTH; off <<= 1) {
+    SPart o;
+    o.m = __shfl_xor_sync(0xffffffffu, p.m, off);
+    o.s = __shfl_xor_sync(0xffffffffu, p.s, off);
+    p = merge(p, o);
+  }
+  return p;
+}
+
+// Thread partial: max of its values, then v <- exp(v - max) in place and
+// their sum (four accumulators).
+template <int NV, int VEC, bool FULL>
+__device__ __forceinline__ SPart thread_part(float (&v)[NV][VEC], const bool (&ok)[NV]) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (FULL || ok[k])
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) mx = fmaxf(mx, v[k][e]);
+  // a slice that is all -inf contributes exp(-inf) = 0, not exp(NaN)
+  const float mb = mx == -INFINITY ? 0.f : mx;
+  constexpr int L = VEC >= 4 ? 4 : VEC;
+  float acc[L];
+#pragma unroll
+  for (int l = 0; l < L; ++l) acc[l] = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    if (FULL || ok[k]) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        v[k][e] = __expf(v[k][e] - mb);
+        acc[e % L] += v[k][e];
+      }
+    }
+  }
+  float s = acc[0];
+#pragma unroll
+  for (int l = 1; l < L; ++l) s += acc[l];
+  return SPart{mx, s};
+}
+
+// ------------------------------------------------------ warp per row
+constexpr int kWarpCtaThreads = 256;
+constexpr int kRowsPerCta = kWarpCtaThreads / 32;
+
+template <int DT, int NV, bool VECTOR, bool FULL>
+__global__ void __launch_bounds__(kWarpCtaThreads, 2) k_softmax_warp(const RowArgs p) {
+  using IO = Io<DT>;
+  constexpr int VEC = VECTOR ? IO::kVec : 1;
+  constexpr int S = IO::kBytes;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
+  pdl_trigger();
+  pdl_wait();
+  if (row >= p.rows) return;
+  const int nvec = p.H / VEC;
+  const int64_t base = row * static_cast<int64_t>(p.H);
+
+  bool ok[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) ok[k] = FULL || (lane + 32 * k) < nvec;
+  float v[NV][VEC];
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
+
+  if constexpr (VECTOR) {
+    const char* xrow = static_cast<const char*>(p.x) + base * S;
+    uint4 xv[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (ok[k]) xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(lane + 32 * k) * 16);
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (ok[k]) IO::unpack(xv[k], v[k]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (ok[k]) v[k][0] = IO::load1(p.x, base + lane + 32 * k);
+  }
+
+  const SPart mine = thread_part<NV, VEC, FULL>(v, ok);
+  const SPart tot = butterfly<32>(mine);
+  const float f = rescale(mine.m, tot.m) / tot.s;
+
+  if constexpr (VECTOR) {
+    char* yrow = static_cast<char*>(p.y) + base * S;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (ok[k]) {
+        float o[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] = v[k][e] * f;
+        st_stream_v4(yrow + static_cast<int64_t>(lane + 32 * k) * 16, IO::pack(o));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (ok[k]) IO::store1(p.y, base + lane + 32 * k, v[k][0] * f);
+  }
+}
+
+// ------------------------------------------------------ CTA per row (TMA)
+template <int DT, int THREADS, int NV, bool FULL>
+__global__ void __launch_bounds__(THREADS) k_softmax_cta(const RowArgs p) {
+  using IO = Io<DT>;
+  constexpr int VEC = IO::kVec;
+  constexpr int S = IO::kBytes;
+  constexpr int NW = THREADS / 32;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nvec = p.H / VEC;
+  const uint32_t row_bytes = static_cast<uint32_t>(p.H) * S;  // multiple of 16
+  const uint32_t rb = (row_bytes + 127u) & ~127u;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + rb);
+  SPart* red = reinterpret_cast<SPart*>(smem + rb + 16);  // [2][NW]
+  const uint32_t xs = smem_addr(smem);
+  const uint32_t bar_a = smem_addr(bar);
+
+  bool ok[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) ok[k] = FULL || (tid + THREADS * k) < nvec;
+
+  if (tid == 0) {
+    mbar_init(bar_a, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint64_t policy = policy_evict_first();
+  pdl_trigger();
+  pdl_wait();
+
+  const int64_t stride = gridDim.x;
+  int64_t row = blockIdx.x;
+  auto issue = [&](int64_t rr) {
+    mbar_arrive_expect_tx(bar_a, row_bytes);
+    bulk_g2s(xs, static_cast<const char*>(p.x) + rr * static_cast<int64_t>(row_bytes), row_bytes,
+             bar_a, policy);
+  };
+  if (tid == 0 && row < p.rows) issue(row);
+
+  for (int64_t it = 0; row < p.rows; ++it, row += stride) {
+    const int64_t base = row * static_cast<int64_t>(p.H);
+    const bool timed_out = !mbar_wait_bounded(bar_a, static_cast<uint32_t>(it & 1), p.wait_limit_ns);
+    float v[NV][VEC];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
+      if (ok[k]) IO::unpack(ld_shared_v4(xs + (tid + THREADS * k) * 16), v[k]);
+    }
+    const SPart mine = thread_part<NV, VEC, FULL>(v, ok);
+    const SPart wp = butterfly<32>(mine);
+    SPart* rbuf = red + (it & 1) * NW;
+    if (lane == 0) rbuf[warp] = wp;
+    // every thread has its slice in registers: the stage may be refilled
+    if (__syncthreads_or(timed_out)) {
+      if (tid == 0) {
+        atomicExch(&g_softmax_error, ADDLN_ERR_DEVICE_TIMEOUT);
+        mbar_wait_bounded(bar_a, static_cast<uint32_t>(it & 1), 1000000000ull);
+      }
+      return;
+    }
+    if (tid == 0 && row + stride < p.rows) issue(row + stride);
+    const SPart tot = butterfly<NW>(rbuf[lane % NW]);
+    const float f = rescale(mine.m, tot.m) / tot.s;
+    char* yrow = static_cast<char*>(p.y) + base * S;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (ok[k]) {
+        float o[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] = v[k][e] * f;
+        st_stream_v4(yrow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::pack(o));
+      }
+    }
+  }
+}
+
+// ------------------------------------------------ CTA per row, elements
+// Misaligned rows: element loads; each thread keeps exp(x_j - m_t) of its own
+// elements (j = tid + THREADS*k) in shared memory.  Every store of a row
+// follows the row's barrier, so y may be x.
+template <int DT, int THREADS>
+__global__ void __launch_bounds__(THREADS) k_softmax_scalar(const RowArgs p) {
+  using IO = Io<DT>;
+  constexpr int NW = THREADS / 32;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int H = p.H;
+  float* se = reinterpret_cast<float*>(smem);
+  SPart* red = reinterpret_cast<SPart*>(smem + ((static_cast<uint32_t>(H) * 4u + 127u) & ~127u));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();
+  pdl_wait();
+  int64_t it = 0;
+  for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
+    const int64_t base = row * static_cast<int64_t>(H);
+    float mx = -INFINITY;
+#pragma unroll 8
+    for (int j = tid; j < H; j += THREADS) {
+      const float a = IO::load1(p.x, base + j);
+      se[j] = a;
+      mx = fmaxf(mx, a);
+    }
+    const float mb = mx == -INFINITY ? 0.f : mx;
+    float s = 0.f;
+    for (int j = tid; j < H; j += THREADS) {
+      const float e = __expf(se[j] - mb);
+      se[j] = e;
+      s += e;
+    }
+    const SPart mine{mx, s};
+    const SPart wp = butterfly<32>(mine);
+    SPart* rbuf = red + (it & 1) * NW;
+    if (lane == 0) rbuf[warp] = wp;
+    __syncthreads();
+    const SPart tot = butterfly<NW>(rbuf[lane % NW]);
+    const float f = rescale(mine.m, tot.m) / tot.s;
+#pragma unroll 4
+    for (int j = tid; j < H; j += THREADS) IO::store1(p.y, base + j, se[j] * f);
+  }
+}
+
+// ------------------------------------------------------------------ host
+namespace {
+
+struct Key {
+  const void* f;
+  int device, smem;
+  bool operator==(const Key& o) const { return f == o.f && device == o.device && smem == o.smem; }
+};
+struct KeyHash {
+  size_t operator()(const Key& k) const {
+    return std::hash<const void*>()(k.f) ^ (static_cast<size_t>(k.device) << 20) ^
+           (static_cast<size_t>(k.smem) << 28);
+  }
+};
+std::mutex g_mu;
+std::unordered_map<Key, int, KeyHash> g_occ;
+
+int resident(const void* f, int threads, int smem, const DeviceInfo& dev) {
+  const Key key{f, dev.device, smem};
+  {
+    std::lock_guard<std::mutex> g(g_mu);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+  }
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return -1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, threads, smem) != cudaSuccess) return -1;
+  std::lock_guard<std::mutex> g(g_mu);
+  g_occ[key] = n;
+  return n;
+}
+
+int64_t grid_for(int64_t rows, int per_sm, const LaunchCtx& c) {
+  int64_t g = static_cast<int64_t>(per_sm) * c.dev.sms;
+  if (c.grid_cap > 0) g = c.grid_cap;
+  if (g > 0x7fffffff) g = 0x7fffffff;
+  return rows < g ? rows : g;
+}
+
+template <int DT, int NV, bool VECTOR>
+int warp_launch(const RowArgs& p, const LaunchCtx& c) {
+  const int64_t blocks = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
+  if (blocks > 0x7fffffff) return ADDLN_ERR_UNSUPPORTED;
+  constexpr int VEC = VECTOR ? Io<DT>::kVec : 1;
+  const bool full = p.H / VEC == 32 * NV;
+  const dim3 grid(static_cast<unsigned>(blocks));
+  const cudaError_t e =
+      full ? launch_kernel(k_softmax_warp<DT, NV, VECTOR, true>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p)
+           : launch_kernel(k_softmax_warp<DT, NV, VECTOR, false>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p);
+  return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+}
+
+template <int DT>
+int warp_dispatch(bool vec, const RowArgs& p, const LaunchCtx& c, const char** name) {
+  if (vec) {
+    constexpr int VEC = Io<DT>::kVec;
+    const int nv = (p.H / VEC + 31) / 32;
+    if (nv <= 1) { *name = "softmax_warp_vec_nv1"; return warp_launch<DT, 1, true>(p, c); }
+    if (nv <= 2) { *name = "softmax_warp_vec_nv2"; return warp_launch<DT, 2, true>(p, c); }
+    if (nv <= 4) { *name = "softmax_warp_vec_nv4"; return warp_launch<DT, 4, true>(p, c); }
+    if constexpr (VEC == 4)
+      if (nv <= 8) { *name = "softmax_warp_vec_nv8"; return warp_launch<DT, 8, true>(p, c); }
+    return ADDLN_ERR_UNSUPPORTED;
+  }
+  const int nv = (p.H + 31) / 32;
+  if (nv <= 4) { *name = "softmax_warp_scalar_nv4"; return warp_launch<DT, 4, false>(p, c); }
+  if (nv <= 8) { *name = "softmax_warp_scalar_nv8"; return warp_launch<DT, 8, false>(p, c); }
+  if (nv <= 16) { *name = "softmax_warp_scalar_nv16"; return warp_launch<DT, 16, false>(p, c); }
+  if (nv <= 32) { *name = "softmax_warp_scalar_nv32"; return warp_launch<DT, 32, false>(p, c); }
+  return ADDLN_ERR_UNSUPPORTED;
+}
+
+template <int DT, int THREADS, int NV, bool FULL>
+int cta_launch_t(const RowArgs& p, const LaunchCtx& c) {
+  const uint32_t row_bytes = static_cast<uint32_t>(p.H) * Io<DT>::kBytes;
+  const uint32_t smem = ((row_bytes + 127u) & ~127u) + 16u + 2u * (THREADS / 32) * sizeof(SPart);
+  if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
+  const void* f = reinterpret_cast<const void*>(&k_softmax_cta<DT, THREADS, NV, FULL>);
+  const int per_sm = resident(f, THREADS, static_cast<int>(smem), c.dev);
+  if (per_sm < 0) return ADDLN_ERR_CUDA;
+  if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
+  const int64_t grid = grid_for(p.rows, per_sm, c);
+  const cudaError_t e = launch_kernel(k_softmax_cta<DT, THREADS, NV, FULL>,
+                                      dim3(static_cast<unsigned>(grid)), dim3(THREADS), smem,
+                                      c.stream, c.pdl, p);
+  return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+}
+
+template <int DT, int THREADS, int NV>
+int cta_launch(const RowArgs& p, const LaunchCtx& c) {
+  return p.H / Io<DT>::kVec == THREADS * NV ? cta_launch_t<DT, THREADS, NV, true>(p, c)
+                                            : cta_launch_t<DT, THREADS, NV, false>(p, c);
+}
+
+template <int DT>
+int cta_dispatch(const RowArgs& p, const LaunchCtx& c, const char** name) {
+  const int nvec = p.H / Io<DT>::kVec;
+  if (nvec <= 128 * 4) { *name = "softmax_cta_tma_t128_nv4"; return cta_launch<DT, 128, 4>(p, c); }
+  if (nvec <= 256 * 4) { *name = "softmax_cta_tma_t256_nv4"; return cta_launch<DT, 256, 4>(p, c); }
+  if (nvec <= 512 * 4) { *name = "softmax_cta_tma_t512_nv4"; return cta_launch<DT, 512, 4>(p, c); }
+  if (nvec <= 512 * 8) { *name = "softmax_cta_tma_t512_nv8"; return cta_launch<DT, 512, 8>(p, c); }
+  return ADDLN_ERR_UNSUPPORTED;
+}
+
+template <int DT>
+int scalar_launch(const RowArgs& p, const LaunchCtx& c) {
+  constexpr int THREADS = 512;
+  const uint32_t smem = ((static_cast<uint32_t>(p.H) * 4u + 127u) & ~127u) +
+                        2u * (THREADS / 32) * sizeof(SPart);
+  if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
+  const void* f = reinterpret_cast<const void*>(&k_softmax_scalar<DT, THREADS>);
+  const int per_sm = resident(f, THREADS, static_cast<int>(smem), c.dev);
+  if (per_sm < 0) return ADDLN_ERR_CUDA;
+  if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
+  const int64_t grid = grid_for(p.rows, per_sm, c);
+  const cudaError_t e = launch_kernel(k_softmax_scalar<DT, THREADS>, dim3(static_cast<unsigned>(grid)),
+                                      dim3(THREADS), smem, c.stream, c.pdl, p);
+  return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+}
+
+}  // namespace
+}  // namespace sm
+
+int launch_softmax_warp(int dtype, bool vec, const RowArgs& p, const LaunchCtx& c, const char** name) {
+  switch (dtype) {
+    case kF32: return sm::warp_dispatch<kF32>(vec, p, c, name);
+    case kF16: return sm::warp_dispatch<kF16>(vec, p, c, name);
+    case kBF16: return sm::warp_dispatch<kBF16>(vec, p, c, name);
+    default: return ADDLN_ERR_DTYPE;
+  }
+}
+
+int launch_softmax_cta(int dtype, const RowArgs& p, const LaunchCtx& c, const char** name) {
+  switch (dtype) {
+    case kF32: return sm::cta_dispatch<kF32>(p, c, name);
+    case kF16: return sm::cta_dispatch<kF16>(p, c, name);
+    case kBF16: return sm::cta_dispatch<kBF16>(p, c, name);
+    default: return ADDLN_ERR_DTYPE;
+  }
+}
+
+int launch_softmax_scalar(int dtype, const RowArgs& p, const LaunchCtx& c, const char** name) {
+  *name = "softmax_cta_scalar_t512";
+  switch (dtype) {
+    case kF32: return sm::scalar_launch<kF32>(p, c);
+    case kF16: return sm::scalar_launch<kF16>(p, c);
+    case kBF16: return sm::scalar_launch<kBF16>(p, c);
+    default: return ADDLN_ERR_DTYPE;
+  }
+}
+
+int read_and_clear_softmax_error(int* code) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, sm::g_softmax_error, sizeof(int)) != cudaSuccess) return ADDLN_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(sm::g_softmax_error, &zero, sizeof(int)) != cudaSuccess) return ADDLN_ERR_CUDA;
+  *code = v;
+  return ADDLN_OK;
+}
+
+}  // namespace addln

@@ -82,3 +82,24 @@ def assert_stats(mean_gpu, rstd_gpu, mean_ref, rstd_ref, what=""):
         raise AssertionError(
             f"{what}: {int(badm.sum())} mean / {int(badr.sum())} rstd out of bound; row {i}: "
             f"mean gpu={mg[i]!r} ref={mean_ref[i]!r}, rstd gpu={rg[i]!r} ref={rstd_ref[i]!r}")
+
+
+def softmax_violations(y_gpu, y_ref: np.ndarray, dtype: str) -> np.ndarray:
+    """Softmax bound: fp32 |dy| <= 1e-5 |y| + 1e-12 (fp32 arithmetic and the
+    hardware exponential give a relative error well under 1e-5 wherever y
+    exceeds 1e-30); fp16 / bf16 within one unit in the last place of the
+    exact value plus that relative term (a faithful rounding)."""
+    yg = to_f64(y_gpu)
+    err = np.abs(yg - y_ref)
+    bound = 1e-5 * np.abs(y_ref) + (1e-12 if dtype == "fp32" else ulp(y_ref, dtype))
+    return ~(err <= bound)
+
+
+def assert_softmax(y_gpu, y_ref, dtype, what=""):
+    bad = softmax_violations(y_gpu, y_ref, dtype)
+    if bad.any():
+        yg = to_f64(y_gpu)
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} softmax outputs out of bound; first "
+            + ", ".join(f"{tuple(i)} gpu={yg[tuple(i)]!r} ref={y_ref[tuple(i)]!r}" for i in idx))

@@ -43,7 +43,8 @@ def header_defines():
 
 def test_header_declares_the_expected_entry_points():
     assert header_functions() == sorted([
-        "add_layernorm_fwd", "add_fwd", "layernorm_fwd", "addln_strerror", "addln_max_hidden",
+        "add_layernorm_fwd", "add_fwd", "layernorm_fwd", "softmax_fwd", "addln_strerror",
+        "addln_max_hidden",
         "addln_get_device_error", "addln_set_force_path", "addln_set_wait_limit_ns",
         "addln_set_grid_cap", "addln_set_pdl", "addln_set_cta_shape", "addln_last_path"])
 
@@ -160,6 +161,13 @@ def test_alias_rules(lib):
                              1e-5, 0, None) == b.ERR_ALIAS
     assert lib.layernorm_fwd(x, None, BASE + 0x2100000, y, None, None, rows, H, 1e-5, 0,
                              None) == b.ERR_NULL
+    # softmax
+    assert lib.softmax_fwd(x, x + 4, rows, H, 0, None) == b.ERR_ALIAS
+    assert lib.softmax_fwd(None, y, rows, H, 0, None) == b.ERR_NULL
+    assert lib.softmax_fwd(x, y, rows, 0, 0, None) == b.ERR_SHAPE
+    assert lib.softmax_fwd(x, y, rows, H, 4, None) == b.ERR_DTYPE
+    assert lib.softmax_fwd(x, y, rows, 32769, 1, None) == b.ERR_SHAPE
+    assert lib.softmax_fwd(None, None, 0, H, 0, None) == b.OK
 
 
 def test_missing_library_fails_loudly(tmp_path):
