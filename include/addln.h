@@ -184,6 +184,10 @@ int addln_set_cta_shape(int threads, int stages);
  * this host thread launched (static text; "none" before the first launch). */
 const char *addln_last_path(void);
 
+/* Text of the CUDA runtime error behind the last ADDLN_ERR_LAUNCH returned on
+ * this host thread (static text; "none" if there was none). */
+const char *addln_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

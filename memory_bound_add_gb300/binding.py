@@ -45,6 +45,7 @@ SIGNATURES = {
     "addln_set_pdl": (ctypes.c_int, [ctypes.c_int]),
     "addln_set_cta_shape": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "addln_last_path": (ctypes.c_char_p, []),
+    "addln_last_cuda_error": (ctypes.c_char_p, []),
 }
 
 _lib = None
@@ -54,7 +55,10 @@ _lock = threading.Lock()
 class AddLNError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {strerror(code)} (code {code})")
+        msg = f"{where}: {strerror(code)} (code {code})"
+        if code in (ERR_LAUNCH, ERR_CUDA):
+            msg += f": {lib().addln_last_cuda_error().decode()}"
+        super().__init__(msg)
 
 
 def lib():
@@ -232,6 +236,10 @@ def addln_set_cta_shape(threads: int, stages: int) -> int:
 
 def addln_last_path() -> str:
     return lib().addln_last_path().decode()
+
+
+def addln_last_cuda_error() -> str:
+    return lib().addln_last_cuda_error().decode()
 
 
 def addln_strerror(code: int) -> str:

@@ -83,6 +83,7 @@ static int launch_add_t(const void* x, const void* r, void* a, int64_t n, const 
     e = launch_kernel(k_add_scalar<DT>, dim3(static_cast<unsigned>(blocks)), dim3(kAddThreads), 0,
                       c.stream, c.pdl, x, r, a, n);
   }
+  if (e != cudaSuccess) note_cuda_error(static_cast<int>(e));
   return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
 

@@ -32,6 +32,7 @@ std::atomic<int> g_pdl{1};
 std::atomic<int> g_cta_threads{0};
 std::atomic<int> g_stages{0};
 thread_local const char* g_last_path = "none";
+thread_local int g_last_cuda_error = 0;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
@@ -175,7 +176,7 @@ int run_softmax(const RowArgs& p, int dtype, void* stream) {
   c.stream = stream;
   c.grid_cap = g_grid_cap.load(std::memory_order_relaxed);
   c.pdl = g_pdl.load(std::memory_order_relaxed) != 0;
-  c.cta_threads = 0;
+  c.cta_threads = g_cta_threads.load(std::memory_order_relaxed);
   c.stages = 0;
   const int rc = device_info(&c.dev);
   if (rc != ADDLN_OK) return rc;
@@ -211,6 +212,8 @@ int run_softmax(const RowArgs& p, int dtype, void* stream) {
 }
 
 }  // namespace
+
+void addln::note_cuda_error(int err) { g_last_cuda_error = err; }
 
 extern "C" {
 
@@ -319,5 +322,10 @@ int addln_set_cta_shape(int threads, int stages) {
 }
 
 const char* addln_last_path(void) { return g_last_path; }
+
+const char* addln_last_cuda_error(void) {
+  return g_last_cuda_error == 0 ? "none"
+                                : cudaGetErrorString(static_cast<cudaError_t>(g_last_cuda_error));
+}
 
 }  // extern "C"

@@ -71,6 +71,10 @@ int launch_softmax_cta(int dtype, const RowArgs& p, const LaunchCtx& c, const ch
 int launch_softmax_scalar(int dtype, const RowArgs& p, const LaunchCtx& c, const char** path_name);
 int read_and_clear_softmax_error(int* code);
 
+// Remembers the CUDA error behind the last ADDLN_ERR_LAUNCH / ADDLN_ERR_CUDA
+// on this host thread (an int cudaError_t; 0 = none).
+void note_cuda_error(int err);
+
 // Device error word (set by a kernel whose bounded wait ran out).
 int read_and_clear_device_error(void* stream, int* code);
 

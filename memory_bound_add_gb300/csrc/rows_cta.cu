@@ -360,8 +360,11 @@ int resident_ctas(const void* f, int threads, int smem, const DeviceInfo& dev) {
     auto it = g_occ.find(key);
     if (it != g_occ.end()) return it->second;
   }
+  // The limit is per function: raise it once to the device's opt-in maximum
+  // (never to this launch's size, which a later, larger launch would exceed).
   if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin) !=
+          cudaSuccess)
     return -1;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, threads, smem) != cudaSuccess) return -1;
@@ -405,6 +408,7 @@ int launch_row_t(const RowArgs& p, const LaunchCtx& c) {
   const cudaError_t e = launch_kernel(k_cta_row<DT, THREADS, NV, TMA, FULL>,
                                       dim3(static_cast<unsigned>(grid)), dim3(THREADS), smem,
                                       c.stream, c.pdl, p, stages);
+  if (e != cudaSuccess) note_cuda_error(static_cast<int>(e));
   return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
 
@@ -455,6 +459,7 @@ int launch_scalar_impl(const RowArgs& p, const LaunchCtx& c) {
   const int64_t grid = persistent_grid(p.rows, per_sm, c);
   const cudaError_t e = launch_kernel(k_cta_scalar<DT, THREADS>, dim3(static_cast<unsigned>(grid)),
                                       dim3(THREADS), smem, c.stream, c.pdl, p);
+  if (e != cudaSuccess) note_cuda_error(static_cast<int>(e));
   return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
 

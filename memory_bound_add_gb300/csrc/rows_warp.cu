@@ -153,6 +153,7 @@ static int launch(const RowArgs& p, const LaunchCtx& c) {
   const cudaError_t e =
       full ? launch_kernel(k_warp_row<DT, NV, VECTOR, true>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p)
            : launch_kernel(k_warp_row<DT, NV, VECTOR, false>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p);
+  if (e != cudaSuccess) note_cuda_error(static_cast<int>(e));
   return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
 

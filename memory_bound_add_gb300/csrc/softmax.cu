@@ -17,8 +17,9 @@
 // Kernels: one warp per row for H <= 1024 (16-byte vector or element loads);
 // one CTA per row for longer rows, the row staged into shared memory by a TMA
 // bulk copy on a bounded mbarrier wait (persistent grid, one row staged per
-// CTA), or element loads into shared memory when rows are not 16-byte
-// aligned.
+// CTA; the row then held in registers, or for the longest rows re-read from
+// the staged copy), or element loads into shared memory when rows are not
+// 16-byte aligned.
 #include <math.h>
 
 #include <mutex>
@@ -235,6 +236,93 @@ __global__ void __launch_bounds__(THREADS) k_softmax_cta(const RowArgs p) {
   }
 }
 
+// ------------------------------------------- CTA per row, long rows (TMA)
+// Rows too long to sit in the registers of several CTAs per SM (more than
+// 2048 16-byte vectors) stay in their staged shared-memory copy and are read
+// twice: pass 1 keeps a running (max, sum of exp) per thread, rescaling the
+// sum when the maximum grows; pass 2 writes exp(x - M) / S.  Two exponentials
+// per element, but a quarter of the registers, so three CTAs (rows) per SM
+// stream instead of one.
+template <int DT, int THREADS>
+__global__ void __launch_bounds__(THREADS) k_softmax_cta_smem(const RowArgs p) {
+  using IO = Io<DT>;
+  constexpr int VEC = IO::kVec;
+  constexpr int S = IO::kBytes;
+  constexpr int NW = THREADS / 32;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nvec = p.H / VEC;
+  const uint32_t row_bytes = static_cast<uint32_t>(p.H) * S;  // multiple of 16
+  const uint32_t rb = (row_bytes + 127u) & ~127u;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + rb);
+  SPart* red = reinterpret_cast<SPart*>(smem + rb + 16);  // [2][NW]
+  const uint32_t xs = smem_addr(smem);
+  const uint32_t bar_a = smem_addr(bar);
+
+  if (tid == 0) {
+    mbar_init(bar_a, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint64_t policy = policy_evict_first();
+  pdl_trigger();
+  pdl_wait();
+
+  const int64_t stride = gridDim.x;
+  int64_t row = blockIdx.x;
+  auto issue = [&](int64_t rr) {
+    mbar_arrive_expect_tx(bar_a, row_bytes);
+    bulk_g2s(xs, static_cast<const char*>(p.x) + rr * static_cast<int64_t>(row_bytes), row_bytes,
+             bar_a, policy);
+  };
+  if (tid == 0 && row < p.rows) issue(row);
+
+  for (int64_t it = 0; row < p.rows; ++it, row += stride) {
+    const bool timed_out = !mbar_wait_bounded(bar_a, static_cast<uint32_t>(it & 1), p.wait_limit_ns);
+    // pass 1: running max and rescaled exp-sum over this thread's vectors
+    SPart mine{-INFINITY, 0.f};
+    for (int c = tid; c < nvec; c += THREADS) {
+      float v[VEC];
+      IO::unpack(ld_shared_v4(xs + c * 16), v);
+      float m8 = v[0];
+#pragma unroll
+      for (int e = 1; e < VEC; ++e) m8 = fmaxf(m8, v[e]);
+      const float mn = fmaxf(mine.m, m8);
+      const float mb = mn == -INFINITY ? 0.f : mn;
+      float s8 = 0.f;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) s8 += __expf(v[e] - mb);
+      mine.s = mine.s * rescale(mine.m, mn) + s8;
+      mine.m = mn;
+    }
+    const SPart wp = butterfly<32>(mine);
+    SPart* rbuf = red + (it & 1) * NW;
+    if (lane == 0) rbuf[warp] = wp;
+    if (__syncthreads_or(timed_out)) {
+      if (tid == 0) {
+        atomicExch(&g_softmax_error, ADDLN_ERR_DEVICE_TIMEOUT);
+        mbar_wait_bounded(bar_a, static_cast<uint32_t>(it & 1), 1000000000ull);
+      }
+      return;
+    }
+    const SPart tot = butterfly<NW>(rbuf[lane % NW]);
+    const float mb = tot.m == -INFINITY ? 0.f : tot.m;
+    const float inv = 1.0f / tot.s;
+    // pass 2: normalise from the staged copy
+    char* yrow = static_cast<char*>(p.y) + row * static_cast<int64_t>(row_bytes);
+    for (int c = tid; c < nvec; c += THREADS) {
+      float v[VEC];
+      IO::unpack(ld_shared_v4(xs + c * 16), v);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) v[e] = __expf(v[e] - mb) * inv;
+      st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::pack(v));
+    }
+    // every thread is done with the staged row before it is refilled
+    __syncthreads();
+    if (tid == 0 && row + stride < p.rows) issue(row + stride);
+  }
+}
+
 // ------------------------------------------------ CTA per row, elements
 // Misaligned rows: element loads; each thread keeps exp(x_j - m_t) of its own
 // elements (j = tid + THREADS*k) in shared memory.  Every store of a row
@@ -303,8 +391,11 @@ int resident(const void* f, int threads, int smem, const DeviceInfo& dev) {
     auto it = g_occ.find(key);
     if (it != g_occ.end()) return it->second;
   }
+  // The limit is per function: raise it once to the device's opt-in maximum
+  // (never to this launch's size, which a later, larger launch would exceed).
   if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin) !=
+          cudaSuccess)
     return -1;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, threads, smem) != cudaSuccess) return -1;
@@ -330,6 +421,7 @@ int warp_launch(const RowArgs& p, const LaunchCtx& c) {
   const cudaError_t e =
       full ? launch_kernel(k_softmax_warp<DT, NV, VECTOR, true>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p)
            : launch_kernel(k_softmax_warp<DT, NV, VECTOR, false>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p);
+  if (e != cudaSuccess) note_cuda_error(static_cast<int>(e));
   return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
 
@@ -366,6 +458,7 @@ int cta_launch_t(const RowArgs& p, const LaunchCtx& c) {
   const cudaError_t e = launch_kernel(k_softmax_cta<DT, THREADS, NV, FULL>,
                                       dim3(static_cast<unsigned>(grid)), dim3(THREADS), smem,
                                       c.stream, c.pdl, p);
+  if (e != cudaSuccess) note_cuda_error(static_cast<int>(e));
   return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
 
@@ -376,13 +469,38 @@ int cta_launch(const RowArgs& p, const LaunchCtx& c) {
 }
 
 template <int DT>
+int smem_launch(const RowArgs& p, const LaunchCtx& c) {
+  constexpr int THREADS = 256;
+  const uint32_t row_bytes = static_cast<uint32_t>(p.H) * Io<DT>::kBytes;
+  const uint32_t smem = ((row_bytes + 127u) & ~127u) + 16u + 2u * (THREADS / 32) * sizeof(SPart);
+  if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
+  const void* f = reinterpret_cast<const void*>(&k_softmax_cta_smem<DT, THREADS>);
+  const int per_sm = resident(f, THREADS, static_cast<int>(smem), c.dev);
+  if (per_sm < 0) return ADDLN_ERR_CUDA;
+  if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
+  const int64_t grid = grid_for(p.rows, per_sm, c);
+  const cudaError_t e = launch_kernel(k_softmax_cta_smem<DT, THREADS>,
+                                      dim3(static_cast<unsigned>(grid)), dim3(THREADS), smem,
+                                      c.stream, c.pdl, p);
+  if (e != cudaSuccess) note_cuda_error(static_cast<int>(e));
+  return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+}
+
+// Rows up to 2048 vectors: registers hold the row; longer rows: the staged
+// copy holds it (k_softmax_cta_smem).  cta_shape threads = 512 forces the
+// register variant for the longest rows too (comparison).
+template <int DT>
 int cta_dispatch(const RowArgs& p, const LaunchCtx& c, const char** name) {
   const int nvec = p.H / Io<DT>::kVec;
   if (nvec <= 128 * 4) { *name = "softmax_cta_tma_t128_nv4"; return cta_launch<DT, 128, 4>(p, c); }
   if (nvec <= 256 * 4) { *name = "softmax_cta_tma_t256_nv4"; return cta_launch<DT, 256, 4>(p, c); }
   if (nvec <= 512 * 4) { *name = "softmax_cta_tma_t512_nv4"; return cta_launch<DT, 512, 4>(p, c); }
-  if (nvec <= 512 * 8) { *name = "softmax_cta_tma_t512_nv8"; return cta_launch<DT, 512, 8>(p, c); }
-  return ADDLN_ERR_UNSUPPORTED;
+  if (c.cta_threads == 512 && nvec <= 512 * 8) {
+    *name = "softmax_cta_tma_t512_nv8";
+    return cta_launch<DT, 512, 8>(p, c);
+  }
+  *name = "softmax_cta_tma_smem_t256";
+  return smem_launch<DT>(p, c);
 }
 
 template <int DT>
@@ -398,6 +516,7 @@ int scalar_launch(const RowArgs& p, const LaunchCtx& c) {
   const int64_t grid = grid_for(p.rows, per_sm, c);
   const cudaError_t e = launch_kernel(k_softmax_scalar<DT, THREADS>, dim3(static_cast<unsigned>(grid)),
                                       dim3(THREADS), smem, c.stream, c.pdl, p);
+  if (e != cudaSuccess) note_cuda_error(static_cast<int>(e));
   return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
 

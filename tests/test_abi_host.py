@@ -46,7 +46,8 @@ def test_header_declares_the_expected_entry_points():
         "add_layernorm_fwd", "add_fwd", "layernorm_fwd", "softmax_fwd", "addln_strerror",
         "addln_max_hidden",
         "addln_get_device_error", "addln_set_force_path", "addln_set_wait_limit_ns",
-        "addln_set_grid_cap", "addln_set_pdl", "addln_set_cta_shape", "addln_last_path"])
+        "addln_set_grid_cap", "addln_set_pdl", "addln_set_cta_shape", "addln_last_path",
+        "addln_last_cuda_error"])
 
 
 def test_library_exports_every_header_symbol(lib):
@@ -82,6 +83,7 @@ def test_strerror_and_limits(lib):
     assert lib.addln_max_hidden(b.BF16) == 32768
     assert lib.addln_max_hidden(7) == b.ERR_DTYPE
     assert lib.addln_last_path() == b"none"
+    assert lib.addln_last_cuda_error() == b"none"
 
 
 def test_force_path_setter(lib):

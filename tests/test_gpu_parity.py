@@ -396,3 +396,13 @@ def test_tma_tuning_shapes(threads, stages):
             check(w, d, out, f"tma t{threads} s{stages} cap{cap}")
     finally:
         mba.addln_set_cta_shape(0, 0)
+
+
+def test_shared_memory_sizes_in_any_order():
+    # the same kernels at large, small, then large shared-memory footprints
+    for H in (32768, 12288, 32768, 8192, 30000):
+        w = synth.custom(3, H, "bf16", want_resid=True, want_stats=True)
+        d = synth.make_inputs(w, seed=H)
+        for path in ("auto", "scalar"):
+            out = run_fused(d, PATHS[path])
+            check(w, d, out, f"order H={H} {path} {out['path']}")

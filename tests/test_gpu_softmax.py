@@ -162,3 +162,29 @@ def test_full_size_sampled_rows(name):
                                      g.choice(w.rows, size=min(128, w.rows), replace=False)]))
     check(d["x"], w.dtype, y, f"{name} full size ({p})", rows=rows)
     assert torch.isfinite(y).all()
+
+
+def test_shared_memory_sizes_in_any_order():
+    # large, small, then large again on the same kernels: the dynamic shared
+    # memory limit of a kernel must never be left below a later launch's need
+    for H in (32000, 12288, 32000, 2048, 30000):
+        w = synth.custom(3, H, "bf16", x_dist=(0.0, 2.0), op="softmax")
+        d = synth.make_inputs(w, seed=H)
+        for path in ("cta_tma", "scalar"):
+            y, p = run(d["x"], PATHS[path])
+            check(d["x"], "bf16", y, f"order H={H} {p}")
+
+
+@pytest.mark.parametrize("threads", [0, 512])
+def test_long_rows_both_variants(threads):
+    # 0: the staged row is re-read from shared memory (two passes);
+    # 512: the row is held in registers by 512 threads x 8 vectors
+    w = synth.with_rows(synth.get("softmax_vocab_4096x32000_bf16"), 23)
+    d = synth.make_inputs(w, seed=5)
+    prev = mba.addln_set_cta_shape(threads, 0)
+    try:
+        y, p = run(d["x"])
+    finally:
+        mba.addln_set_cta_shape(0, 0)
+    assert p == ("softmax_cta_tma_t512_nv8" if threads == 512 else "softmax_cta_tma_smem_t256")
+    check(d["x"], w.dtype, y, p)
