@@ -17,5 +17,6 @@ from .oracle import (
     oracle_layernorm,
     oracle_add_layernorm,
     oracle_softmax,
+    oracle_bias_gelu_residual,
     load,
 )

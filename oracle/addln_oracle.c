@@ -35,6 +35,12 @@
  * in the page's order: a max pass, an exp-sum pass, a divide pass; fp64
  * throughout, libm exp.
  *
+ * Bias + GELU + residual ("算子融合的收益量化", the three-kernel chain of the
+ * diagram before section 1: BiasAdd, GELU, Residual), per element:
+ *   v_ij = x_ij + bias_j
+ *   Y_ij = GELU(v_ij) + r_ij,   GELU(v) = v * Phi(v) = v/2 * (1 + erf(v / sqrt 2))
+ * (the exact, erf form; the page names no variant), fp64 with libm erf.
+ *
  * dtype codes: 0 = IEEE binary32, 1 = IEEE binary16, 2 = bfloat16.
  * Return value: 0 on success, -1 on a bad argument.
  *
@@ -258,5 +264,25 @@ int oracle_softmax(const void *x, int dtype, int64_t rows, int64_t H, double *y,
         softmax_row(row, H, y + i * H, row_max ? row_max + i : NULL, row_sum ? row_sum + i : NULL);
     }
     free(row);
+    return 0;
+}
+
+static double gelu_exact(double v)
+{
+    return 0.5 * v * (1.0 + erf(v / sqrt(2.0)));
+}
+
+/* Y = GELU(X + bias) + R over [rows, H]; bias fp32 [H]; y fp64 [rows, H]. */
+int oracle_bias_gelu_residual(const void *x, const void *r, int dtype, const float *bias,
+                              int64_t rows, int64_t H, double *y)
+{
+    if (bad_dtype(dtype) || rows < 0 || H <= 0 || (rows > 0 && (!x || !r || !bias || !y)))
+        return -1;
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t j = 0; j < H; ++j) {
+            const int64_t k = i * H + j;
+            const double v = decode_at(x, dtype, k) + (double)bias[j];
+            y[k] = gelu_exact(v) + decode_at(r, dtype, k);
+        }
     return 0;
 }

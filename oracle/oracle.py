@@ -35,8 +35,9 @@ def load():
             lib.oracle_add_layernorm.argtypes = [_P, _P, ctypes.c_int, _P, _P, _I64, _I64,
                                                  ctypes.c_double, ctypes.c_int, _P, _P, _P, _P]
             lib.oracle_softmax.argtypes = [_P, ctypes.c_int, _I64, _I64, _P, _P, _P]
+            lib.oracle_bias_gelu_residual.argtypes = [_P, _P, ctypes.c_int, _P, _I64, _I64, _P]
             for f in ("oracle_decode", "oracle_round", "oracle_add", "oracle_layernorm",
-                      "oracle_add_layernorm", "oracle_softmax"):
+                      "oracle_add_layernorm", "oracle_softmax", "oracle_bias_gelu_residual"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -143,3 +144,16 @@ def oracle_softmax(x, dtype: str) -> dict:
     _check(load().oracle_softmax(_ptr(xs), _DT[dtype], rows, H, _ptr(y), _ptr(mx), _ptr(sm)),
            "oracle_softmax")
     return {"y": y, "max": mx, "sum": sm}
+
+
+def oracle_bias_gelu_residual(x, r, bias, dtype: str) -> np.ndarray:
+    """Y = GELU(X + bias) + R (exact erf GELU) in fp64, [rows, H]."""
+    xs, rs = _raw(x, dtype), _raw(r, dtype)
+    assert xs.shape == rs.shape and xs.ndim == 2
+    rows, H = xs.shape
+    b = _f32(bias)
+    assert b.shape == (H,)
+    y = np.empty((rows, H), dtype=np.float64)
+    _check(load().oracle_bias_gelu_residual(_ptr(xs), _ptr(rs), _DT[dtype], _ptr(b), rows, H,
+                                            _ptr(y)), "oracle_bias_gelu_residual")
+    return y

@@ -42,7 +42,8 @@ class Workload:
     outlier_mag: float = 50.0
     note: str = ""
     shape_bsh: tuple = field(default=None)
-    op: str = "add_layernorm"     # or "softmax" (row softmax of X; R, gamma, beta unused)
+    op: str = "add_layernorm"     # "softmax": row softmax of X (R, gamma, beta unused)
+    #                                 "bias_gelu_residual": GELU(X + bias) + R (bias = beta draw)
 
     @property
     def n_const_rows(self) -> int:
@@ -69,6 +70,8 @@ class Workload:
         s = self.elem_bytes
         if self.op == "softmax":
             return 2 * self.rows * self.H * s
+        if self.op == "bias_gelu_residual":
+            return 3 * self.rows * self.H * s + 4 * self.H
         per_row = 2 * self.H * s + self.H * s * (1 + int(self.want_resid)) + 8 * int(self.want_stats)
         return self.rows * per_row + 8 * self.H
 
@@ -129,6 +132,20 @@ SOFTMAX = [
 ]
 WORKLOADS.update({w.name: w for w in SOFTMAX})
 SOFTMAX_NAMES = [w.name for w in SOFTMAX]
+
+# Bias + GELU + residual ("算子融合的收益量化", the three-kernel diagram): the
+# diagram's 8 MB tensors ([1, 1024, 4096] fp16), and a large bf16 case.  The
+# bias is the beta draw (fp32 [H]); X ~ N(0, 1), R ~ N(0, 0.5).
+BGR = [
+    Workload("bgr_pages_1024x4096_fp16", 1024, 4096, "fp16", 0.0, r_dist=(0.0, 0.5),
+             op="bias_gelu_residual", note="the diagram's 8 MB tensors", shape_bsh=(1, 1024, 4096)),
+    Workload("bgr_large_32768x8192_bf16", 32768, 8192, "bf16", 0.0, r_dist=(0.0, 0.5),
+             op="bias_gelu_residual", note="512 MB tensors", shape_bsh=(8, 4096, 8192)),
+    Workload("bgr_tail_1000x1001_fp32", 1000, 1001, "fp32", 0.0, r_dist=(0.0, 0.5),
+             op="bias_gelu_residual", note="odd H: element path"),
+]
+WORKLOADS.update({w.name: w for w in BGR})
+BGR_NAMES = [w.name for w in BGR]
 
 # The five workloads of the method's scope, in order; the rest are extra tails.
 PRIMARY = [
