@@ -45,6 +45,8 @@ import synth  # noqa: E402
 
 METRIC = "fused Add+LayerNorm effective HBM GB/s and % of GB300 peak; rows/sec"
 METRIC_SOFTMAX = "fused row softmax effective HBM GB/s and % of GB300 peak; rows/sec"
+METRIC_BGR = "fused bias+GELU+residual effective HBM GB/s and % of GB300 peak; rows/sec"
+METRICS = {"add_layernorm": METRIC, "softmax": METRIC_SOFTMAX, "bias_gelu_residual": METRIC_BGR}
 DEFAULT_WORKLOAD = "pages_2048x4096_fp16"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
@@ -247,6 +249,8 @@ def make_sets(w, d, n_sets, dev):
             "a": torch.empty(rows, w.H, dtype=d["x"].dtype, device=dev) if w.want_resid else None,
             "mean": torch.empty(rows, dtype=torch.float32, device=dev) if w.want_stats else None,
             "rstd": torch.empty(rows, dtype=torch.float32, device=dev) if w.want_stats else None,
+            "t": torch.empty(rows, w.H, dtype=d["x"].dtype, device=dev)
+            if w.op == "bias_gelu_residual" else None,
         }
         sets.append(s)
     return sets
@@ -256,12 +260,22 @@ def set_bytes(w):
     s = w.elem_bytes
     if w.op == "softmax":
         return 2 * w.rows * w.H * s
+    if w.op == "bias_gelu_residual":
+        return 4 * w.rows * w.H * s       # X, R, Y and the unfused chain's T
     b = 3 * w.rows * w.H * s
     if w.want_resid:
         b += w.rows * w.H * s
     if w.want_stats:
         b += 8 * w.rows
     return b
+
+
+def unfused_bytes(w):
+    """Minimal bytes of the unfused chain: add + LayerNorm, or for bias +
+    GELU + residual its three kernels (2 + 2 + 3 tensor passes and the bias)."""
+    if w.op == "bias_gelu_residual":
+        return 7 * w.rows * w.H * w.elem_bytes + 4 * w.H
+    return w.unfused_algorithmic_bytes()
 
 
 def capture(step_fn, n_steps, n_sets, offset=0):
@@ -345,12 +359,16 @@ def run_ours(args):
         if w.op == "softmax":
             mba.softmax_fwd(s["x"], s["y"])
             return
+        if w.op == "bias_gelu_residual":
+            mba.bias_gelu_residual_fwd(s["x"], s["r"], beta, s["y"])
+            return
         mba.add_layernorm_fwd(s["x"], s["r"], gamma, beta, s["y"], s["a"], s["mean"], s["rstd"],
                               eps=eps)
 
     fused_step(0)
     torch.cuda.synchronize()
-    path = mba.addln_last_path() if args.kernel == "fused" else "add_vec"
+    path = (mba.addln_last_path() if w.op != "bias_gelu_residual" else "bgr_vec") \
+        if args.kernel == "fused" else "add_vec"
     if mba.addln_get_device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
 
@@ -381,7 +399,7 @@ def run_ours(args):
     achieved = alg / per_launch_s / 1e9
     peak, peak_kind = measured_peak()
     result = {
-        "metric": METRIC if w.op != "softmax" else METRIC_SOFTMAX,
+        "metric": METRICS[w.op],
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": ws,
@@ -427,6 +445,9 @@ def run_ours(args):
     if not args.only_fused and not args.no_unfused and w.op != "softmax":
         def unfused_step(i):
             s = sets[i]
+            if w.op == "bias_gelu_residual":
+                mba.bias_gelu_residual_unfused(s["x"], s["r"], beta, t=s["t"], y=s["y"])
+                return
             a = s["a"] if s["a"] is not None else s["y"]
             mba.add_fwd(s["x"], s["r"], a)
             mba.layernorm_fwd(a, gamma, beta, s["y"], s["mean"], s["rstd"], eps=eps)
@@ -436,10 +457,10 @@ def run_ours(args):
         result["unfused_baseline"] = {
             "value": round(ws * alg * Ku / el_u / 1e9, 2),
             "unit": "GB/s (fused algorithmic bytes / time)",
-            "own_traffic_gbs": round(ws * w.unfused_algorithmic_bytes() * Ku / el_u / 1e9, 2),
+            "own_traffic_gbs": round(ws * unfused_bytes(w) * Ku / el_u / 1e9, 2),
             "ms_per_step": round(el_u / Ku * 1e3, 6),
             "steps": Ku,
-            "gpu_launches": 2 * Ku,
+            "gpu_launches": (3 if w.op == "bias_gelu_residual" else 2) * Ku,
             "fused_speedup": round(el_u / Ku / (elapsed / K), 3),
         }
 
@@ -487,6 +508,11 @@ def run_e2e(mba, w, d, dev, steps, W, barrier, ws):
             hy.copy_(y, non_blocking=True)
             return
         r.copy_(hr, non_blocking=True)
+        if w.op == "bias_gelu_residual":
+            b.copy_(hb, non_blocking=True)
+            mba.bias_gelu_residual_fwd(x, r, b, y)
+            hy.copy_(y, non_blocking=True)
+            return
         g.copy_(hg, non_blocking=True)
         b.copy_(hb, non_blocking=True)
         mba.add_layernorm_fwd(x, r, g, b, y, a, m, s, eps=d["eps"])
@@ -513,7 +539,8 @@ def run_e2e(mba, w, d, dev, steps, W, barrier, ws):
     barrier()
     el = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
     h2d = hx.numel() * hx.element_size() if soft else \
-        (hx.numel() + hr.numel()) * hx.element_size() + 8 * w.H
+        (hx.numel() + hr.numel()) * hx.element_size() + \
+        (4 if w.op == "bias_gelu_residual" else 8) * w.H
     d2h = hy.numel() * hy.element_size() * (2 if w.want_resid else 1) + (8 * w.rows if w.want_stats else 0)
     return {"value": round(whole_job_gbs(ws, w.algorithmic_bytes(), steps, el), 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
@@ -550,6 +577,8 @@ def oracle_rows_call(w, d, lo, hi):
     import oracle
     if w.op == "softmax":
         return oracle.oracle_softmax(d["x"][lo:hi], w.dtype)
+    if w.op == "bias_gelu_residual":
+        return oracle.oracle_bias_gelu_residual(d["x"][lo:hi], d["r"][lo:hi], d["beta"], w.dtype)
     return oracle.oracle_add_layernorm(d["x"][lo:hi], d["r"][lo:hi], d["gamma"], d["beta"],
                                        d["eps"], w.dtype, want_a=w.want_resid,
                                        want_stats=w.want_stats)
@@ -607,7 +636,7 @@ def run_reference(args):
     value = done * per_row / el / 1e9
     sample = f"{rows_per_step} rows of {w.name} per step, single-threaded fp64 C oracle"
     print(json.dumps({
-        "metric": METRIC if w.op != "softmax" else METRIC_SOFTMAX, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws, "steps": K,
+        "metric": METRICS[w.op], "value": round(value, 4), "unit": "GB/s", "n_gpus": ws, "steps": K,
         "warmup": W, "ms_per_step": round(el / K * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",

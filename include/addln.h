@@ -117,6 +117,28 @@ int layernorm_fwd(const void *a, const float *gamma, const float *beta, void *y,
  */
 int softmax_fwd(const void *x, void *y, int64_t rows, int64_t H, int dtype, void *stream);
 
+/*
+ * Fused bias + GELU + residual (the BiasAdd -> GELU -> Residual chain of the
+ * diagram in "算子融合的收益量化", three kernels fused into one):
+ *     Y_ij = GELU(X_ij + bias_j) + R_ij,  GELU(v) = v/2 * (1 + erf(v / sqrt 2))
+ *   x, r  [rows, H] inputs in dtype (required)
+ *   bias  [H] fp32 (required)
+ *   y     [rows, H] output in dtype; may be x or r exactly (in place)
+ * fp32 arithmetic with CUDA's erff; Y rounded to nearest even.  One read of X
+ * and R, one write of Y.  Same conventions and error codes as the calls above.
+ */
+int bias_gelu_residual_fwd(const void *x, const void *r, const float *bias, void *y,
+                           int64_t rows, int64_t H, int dtype, void *stream);
+
+/* Unfused chain, step 1 (the diagram's BiasAdd kernel): T = X + bias per
+ * column, [rows, H] in dtype; t may be x exactly. */
+int bias_add_fwd(const void *x, const float *bias, void *t, int64_t rows, int64_t H, int dtype,
+                 void *stream);
+
+/* Unfused chain, step 2 (the diagram's GELU kernel): U = GELU(T) over n
+ * contiguous elements; u may be t exactly.  Step 3 (Residual) is add_fwd. */
+int gelu_fwd(const void *t, void *u, int64_t n, int dtype, void *stream);
+
 /* Static text for a return code (never NULL). */
 const char *addln_strerror(int code);
 

@@ -12,6 +12,11 @@ from .binding import (  # noqa: F401
     add_then_layernorm,
     softmax_fwd,
     softmax,
+    bias_gelu_residual_fwd,
+    bias_add_fwd,
+    gelu_fwd,
+    bias_gelu_residual,
+    bias_gelu_residual_unfused,
     addln_get_device_error,
     addln_set_force_path,
     addln_set_wait_limit_ns,

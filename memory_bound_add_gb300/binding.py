@@ -36,6 +36,9 @@ SIGNATURES = {
     "layernorm_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_float,
                                      ctypes.c_int, _P]),
     "softmax_fwd": (ctypes.c_int, [_P, _P, _I64, _I64, ctypes.c_int, _P]),
+    "bias_gelu_residual_fwd": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, ctypes.c_int, _P]),
+    "bias_add_fwd": (ctypes.c_int, [_P, _P, _P, _I64, _I64, ctypes.c_int, _P]),
+    "gelu_fwd": (ctypes.c_int, [_P, _P, _I64, ctypes.c_int, _P]),
     "addln_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "addln_max_hidden": (ctypes.c_int64, [ctypes.c_int]),
     "addln_get_device_error": (ctypes.c_int, [_P]),
@@ -203,6 +206,56 @@ def softmax(x, stream=None):
     """Allocate y with PyTorch and run softmax_fwd."""
     y = torch.empty_like(x)
     softmax_fwd(x, y, stream=stream)
+    return y
+
+
+def bias_gelu_residual_fwd(x, r, bias, y, stream=None, rows=None, H=None, dtype=None):
+    """Y = GELU(X + bias) + R in one kernel."""
+    if isinstance(x, torch.Tensor):
+        rows_, H_ = _rows_shape(x)
+        _require(x, "x")
+        _require(r, "r", x.dtype, like=x)
+        _require(y, "y", x.dtype, like=x)
+        _require(bias, "bias", torch.float32)
+        if bias.numel() != H_:
+            raise ValueError(f"bias must have H={H_} elements")
+        rows = rows_ if rows is None else rows
+        H = H_ if H is None else H
+        dtype = DTYPE_CODE[x.dtype] if dtype is None else dtype
+    _check(lib().bias_gelu_residual_fwd(_ptr(x), _ptr(r), _ptr(bias), _ptr(y), int(rows), int(H),
+                                        int(dtype), _stream(stream)), "bias_gelu_residual_fwd")
+
+
+def bias_add_fwd(x, bias, t, stream=None):
+    rows, H = _rows_shape(x)
+    _require(x, "x")
+    _require(t, "t", x.dtype, like=x)
+    _check(lib().bias_add_fwd(_ptr(x), _ptr(bias), _ptr(t), rows, H, DTYPE_CODE[x.dtype],
+                              _stream(stream)), "bias_add_fwd")
+
+
+def gelu_fwd(t, u, stream=None):
+    _require(t, "t")
+    _require(u, "u", t.dtype, like=t)
+    _check(lib().gelu_fwd(_ptr(t), _ptr(u), t.numel(), DTYPE_CODE[t.dtype], _stream(stream)),
+           "gelu_fwd")
+
+
+def bias_gelu_residual(x, r, bias, stream=None):
+    """Allocate Y with PyTorch and run bias_gelu_residual_fwd."""
+    y = torch.empty_like(x)
+    bias_gelu_residual_fwd(x, r, bias, y, stream=stream)
+    return y
+
+
+def bias_gelu_residual_unfused(x, r, bias, t=None, y=None, stream=None):
+    """The three-kernel chain: T = X + bias, T = GELU(T), Y = T + R, each a
+    separate HBM round trip (T is stored in the I/O dtype)."""
+    t = torch.empty_like(x) if t is None else t
+    y = torch.empty_like(x) if y is None else y
+    bias_add_fwd(x, bias, t, stream=stream)
+    gelu_fwd(t, t, stream=stream)
+    add_fwd(t, r, y, stream=stream)
     return y
 
 

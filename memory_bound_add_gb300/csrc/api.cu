@@ -252,6 +252,63 @@ int layernorm_fwd(const void* a, const float* gamma, const float* beta, void* y,
   return run_rows(p, dtype, stream);
 }
 
+namespace {
+int plain_ctx(void* stream, LaunchCtx* c) {
+  c->stream = stream;
+  c->grid_cap = 0;
+  c->pdl = g_pdl.load(std::memory_order_relaxed) != 0;
+  c->cta_threads = 0;
+  c->stages = 0;
+  return device_info(&c->dev);
+}
+}  // namespace
+
+int bias_gelu_residual_fwd(const void* x, const void* r, const float* bias, void* y, int64_t rows,
+                           int64_t H, int dtype, void* stream) {
+  if (!valid_dtype(dtype)) return ADDLN_ERR_DTYPE;
+  if (rows < 0 || H <= 0 || rows > INT64_MAX / (H * 4)) return ADDLN_ERR_SHAPE;
+  if (rows == 0) return ADDLN_OK;
+  if (!x || !r || !bias || !y) return ADDLN_ERR_NULL;
+  const int64_t tb = rows * H * elem_bytes(dtype);
+  const Range ry = range_of(y, tb);
+  if (bad_pair(ry, range_of(x, tb), true) || bad_pair(ry, range_of(r, tb), true) ||
+      bad_pair(ry, range_of(bias, H * 4), false))
+    return ADDLN_ERR_ALIAS;
+  LaunchCtx c;
+  const int rc = plain_ctx(stream, &c);
+  if (rc != ADDLN_OK) return rc;
+  return addln::launch_bias_gelu_residual(dtype, x, r, bias, y, rows, H, c);
+}
+
+int bias_add_fwd(const void* x, const float* bias, void* t, int64_t rows, int64_t H, int dtype,
+                 void* stream) {
+  if (!valid_dtype(dtype)) return ADDLN_ERR_DTYPE;
+  if (rows < 0 || H <= 0 || rows > INT64_MAX / (H * 4)) return ADDLN_ERR_SHAPE;
+  if (rows == 0) return ADDLN_OK;
+  if (!x || !bias || !t) return ADDLN_ERR_NULL;
+  const int64_t tb = rows * H * elem_bytes(dtype);
+  const Range rt = range_of(t, tb);
+  if (bad_pair(rt, range_of(x, tb), true) || bad_pair(rt, range_of(bias, H * 4), false))
+    return ADDLN_ERR_ALIAS;
+  LaunchCtx c;
+  const int rc = plain_ctx(stream, &c);
+  if (rc != ADDLN_OK) return rc;
+  return addln::launch_bias_add(dtype, x, bias, t, rows, H, c);
+}
+
+int gelu_fwd(const void* x, void* u, int64_t n, int dtype, void* stream) {
+  if (!valid_dtype(dtype)) return ADDLN_ERR_DTYPE;
+  if (n < 0 || n > INT64_MAX / 4) return ADDLN_ERR_SHAPE;
+  if (n == 0) return ADDLN_OK;
+  if (!x || !u) return ADDLN_ERR_NULL;
+  const int64_t tb = n * elem_bytes(dtype);
+  if (bad_pair(range_of(u, tb), range_of(x, tb), true)) return ADDLN_ERR_ALIAS;
+  LaunchCtx c;
+  const int rc = plain_ctx(stream, &c);
+  if (rc != ADDLN_OK) return rc;
+  return addln::launch_gelu(dtype, x, u, n, c);
+}
+
 int add_fwd(const void* x, const void* r, void* a, int64_t n, int dtype, void* stream) {
   if (!valid_dtype(dtype)) return ADDLN_ERR_DTYPE;
   if (n < 0 || n > INT64_MAX / 4) return ADDLN_ERR_SHAPE;

@@ -1,0 +1,157 @@
+// Bias + GELU + residual, fused: Y = GELU(X + bias) + R, one read of X and R
+// and one write of Y -- the single fused kernel of the BiasAdd -> GELU ->
+// Residual diagram in "算子融合的收益量化".  GELU is the exact form
+// v * Phi(v) = v/2 * (1 + erf(v / sqrt 2)) with CUDA's erff.  bias is fp32
+// [H], broadcast along rows.
+//
+// Also the two extra steps of the diagram's unfused chain, each its own
+// kernel with its own HBM round trip: T = X + bias and U = GELU(T) (the third
+// step, Y = U + R, is add_fwd).
+//
+// All kernels stream 16-byte vectors grid-stride with four independent
+// vectors in flight per thread; element accesses serve misaligned buffers
+// and rows that are not whole vectors.
+#include "../../include/addln.h"
+#include "common.cuh"
+
+namespace addln {
+namespace ew {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+__device__ __forceinline__ float gelu(float v) {
+  return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+}
+
+// What each element becomes.  kBgr: GELU(x + b) + r; kBias: x + b; kGelu: GELU(x).
+enum Kind { kBgr = 0, kBias = 1, kGelu = 2 };
+
+template <int KIND>
+__device__ __forceinline__ float apply(float x, float r, float b) {
+  if constexpr (KIND == kBgr) return gelu(x + b) + r;
+  if constexpr (KIND == kBias) return x + b;
+  return gelu(x);
+}
+
+// Vector path: every buffer 16-byte aligned, H a multiple of the vector width
+// (so a vector never straddles two rows and its bias slice is aligned).
+template <int DT, int KIND>
+__global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* r, const float* bias,
+                                                     void* y, int64_t nvec, int64_t hvec) {
+  using IO = Io<DT>;
+  constexpr int VEC = IO::kVec;
+  constexpr bool HAS_R = KIND == kBgr;
+  constexpr bool HAS_B = KIND != kGelu;
+  const uint4* xv = static_cast<const uint4*>(x);
+  const uint4* rv = static_cast<const uint4*>(r);
+  uint4* yv = static_cast<uint4*>(y);
+  pdl_trigger();
+  pdl_wait();
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads * kUnroll;
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kThreads * kUnroll + threadIdx.x; i0 < nvec;
+       i0 += step) {
+    uint4 xs[kUnroll], rs[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = i0 + static_cast<int64_t>(u) * kThreads;
+      if (i < nvec) {
+        xs[u] = ld_stream_v4(xv + i);
+        if constexpr (HAS_R) rs[u] = ld_stream_v4(rv + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = i0 + static_cast<int64_t>(u) * kThreads;
+      if (i < nvec) {
+        float f[VEC], g[VEC], b[VEC];
+        IO::unpack(xs[u], f);
+        if constexpr (HAS_R) IO::unpack(rs[u], g);
+        if constexpr (HAS_B) {
+          const float* bp = bias + (i % hvec) * VEC;
+#pragma unroll
+          for (int q = 0; q < VEC / 4; ++q) {
+            const float4 t = ld_param_f4(bp + 4 * q);
+            b[4 * q] = t.x; b[4 * q + 1] = t.y; b[4 * q + 2] = t.z; b[4 * q + 3] = t.w;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+          f[e] = apply<KIND>(f[e], HAS_R ? g[e] : 0.f, HAS_B ? b[e] : 0.f);
+        st_stream_v4(yv + i, IO::pack(f));
+      }
+    }
+  }
+}
+
+// Element path: any alignment and any H.
+template <int DT, int KIND>
+__global__ void __launch_bounds__(kThreads) k_ew_scalar(const void* x, const void* r,
+                                                        const float* bias, void* y, int64_t n,
+                                                        int64_t H) {
+  using IO = Io<DT>;
+  pdl_trigger();
+  pdl_wait();
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; k < n; k += step) {
+    const float xv = IO::load1(x, k);
+    const float rv = KIND == kBgr ? IO::load1(r, k) : 0.f;
+    const float bv = KIND != kGelu ? __ldg(bias + k % H) : 0.f;
+    IO::store1(y, k, apply<KIND>(xv, rv, bv));
+  }
+}
+
+template <int DT, int KIND>
+int launch_t(const void* x, const void* r, const float* bias, void* y, int64_t rows, int64_t H,
+             const LaunchCtx& c) {
+  constexpr int VEC = Io<DT>::kVec;
+  const int64_t n = rows * H;
+  auto al = [](const void* q) { return q == nullptr || (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  const int64_t max_blocks = static_cast<int64_t>(c.dev.sms) * (2048 / kThreads);
+  cudaError_t e;
+  if (H % VEC == 0 && al(x) && al(r) && al(y) && al(bias)) {
+    const int64_t nvec = n / VEC;
+    int64_t blocks = (nvec + kThreads * kUnroll - 1) / (kThreads * kUnroll);
+    if (blocks > max_blocks) blocks = max_blocks;
+    if (blocks < 1) blocks = 1;
+    e = launch_kernel(k_ew_vec<DT, KIND>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
+                      c.stream, c.pdl, x, r, bias, y, nvec, H / VEC);
+  } else {
+    int64_t blocks = (n + kThreads - 1) / kThreads;
+    if (blocks > max_blocks) blocks = max_blocks;
+    if (blocks < 1) blocks = 1;
+    e = launch_kernel(k_ew_scalar<DT, KIND>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
+                      c.stream, c.pdl, x, r, bias, y, n, H);
+  }
+  if (e != cudaSuccess) note_cuda_error(static_cast<int>(e));
+  return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
+}
+
+template <int KIND>
+int launch_kind(int dtype, const void* x, const void* r, const float* bias, void* y, int64_t rows,
+                int64_t H, const LaunchCtx& c) {
+  switch (dtype) {
+    case kF32: return launch_t<kF32, KIND>(x, r, bias, y, rows, H, c);
+    case kF16: return launch_t<kF16, KIND>(x, r, bias, y, rows, H, c);
+    case kBF16: return launch_t<kBF16, KIND>(x, r, bias, y, rows, H, c);
+    default: return ADDLN_ERR_DTYPE;
+  }
+}
+
+}  // namespace ew
+
+int launch_bias_gelu_residual(int dtype, const void* x, const void* r, const float* bias, void* y,
+                              int64_t rows, int64_t H, const LaunchCtx& c) {
+  return ew::launch_kind<ew::kBgr>(dtype, x, r, bias, y, rows, H, c);
+}
+
+int launch_bias_add(int dtype, const void* x, const float* bias, void* y, int64_t rows, int64_t H,
+                    const LaunchCtx& c) {
+  return ew::launch_kind<ew::kBias>(dtype, x, nullptr, bias, y, rows, H, c);
+}
+
+int launch_gelu(int dtype, const void* x, void* y, int64_t n, const LaunchCtx& c) {
+  return ew::launch_kind<ew::kGelu>(dtype, x, nullptr, nullptr, y, 1, n, c);
+}
+
+}  // namespace addln

@@ -71,6 +71,13 @@ int launch_softmax_cta(int dtype, const RowArgs& p, const LaunchCtx& c, const ch
 int launch_softmax_scalar(int dtype, const RowArgs& p, const LaunchCtx& c, const char** path_name);
 int read_and_clear_softmax_error(int* code);
 
+// Bias + GELU + residual (fused) and the two extra steps of its unfused chain.
+int launch_bias_gelu_residual(int dtype, const void* x, const void* r, const float* bias, void* y,
+                              int64_t rows, int64_t H, const LaunchCtx& c);
+int launch_bias_add(int dtype, const void* x, const float* bias, void* y, int64_t rows, int64_t H,
+                    const LaunchCtx& c);
+int launch_gelu(int dtype, const void* x, void* y, int64_t n, const LaunchCtx& c);
+
 // Remembers the CUDA error behind the last ADDLN_ERR_LAUNCH / ADDLN_ERR_CUDA
 // on this host thread (an int cudaError_t; 0 = none).
 void note_cuda_error(int err);

@@ -272,17 +272,25 @@ static double gelu_exact(double v)
     return 0.5 * v * (1.0 + erf(v / sqrt(2.0)));
 }
 
-/* Y = GELU(X + bias) + R over [rows, H]; bias fp32 [H]; y fp64 [rows, H]. */
+/* Y = GELU(X + bias) + R over [rows, H]; bias fp32 [H]; y fp64 [rows, H].
+ * round_intermediates != 0: the three-kernel chain, which stores X + bias and
+ * GELU of it in the I/O dtype (each rounded to nearest even) before the next
+ * step reads them. */
 int oracle_bias_gelu_residual(const void *x, const void *r, int dtype, const float *bias,
-                              int64_t rows, int64_t H, double *y)
+                              int64_t rows, int64_t H, int round_intermediates, double *y)
 {
     if (bad_dtype(dtype) || rows < 0 || H <= 0 || (rows > 0 && (!x || !r || !bias || !y)))
         return -1;
     for (int64_t i = 0; i < rows; ++i)
         for (int64_t j = 0; j < H; ++j) {
             const int64_t k = i * H + j;
-            const double v = decode_at(x, dtype, k) + (double)bias[j];
-            y[k] = gelu_exact(v) + decode_at(r, dtype, k);
+            double v = decode_at(x, dtype, k) + (double)bias[j];
+            if (round_intermediates)
+                v = round_to_dtype(v, dtype);
+            double g = gelu_exact(v);
+            if (round_intermediates)
+                g = round_to_dtype(g, dtype);
+            y[k] = g + decode_at(r, dtype, k);
         }
     return 0;
 }

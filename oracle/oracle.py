@@ -35,7 +35,8 @@ def load():
             lib.oracle_add_layernorm.argtypes = [_P, _P, ctypes.c_int, _P, _P, _I64, _I64,
                                                  ctypes.c_double, ctypes.c_int, _P, _P, _P, _P]
             lib.oracle_softmax.argtypes = [_P, ctypes.c_int, _I64, _I64, _P, _P, _P]
-            lib.oracle_bias_gelu_residual.argtypes = [_P, _P, ctypes.c_int, _P, _I64, _I64, _P]
+            lib.oracle_bias_gelu_residual.argtypes = [_P, _P, ctypes.c_int, _P, _I64, _I64,
+                                                      ctypes.c_int, _P]
             for f in ("oracle_decode", "oracle_round", "oracle_add", "oracle_layernorm",
                       "oracle_add_layernorm", "oracle_softmax", "oracle_bias_gelu_residual"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -146,8 +147,10 @@ def oracle_softmax(x, dtype: str) -> dict:
     return {"y": y, "max": mx, "sum": sm}
 
 
-def oracle_bias_gelu_residual(x, r, bias, dtype: str) -> np.ndarray:
-    """Y = GELU(X + bias) + R (exact erf GELU) in fp64, [rows, H]."""
+def oracle_bias_gelu_residual(x, r, bias, dtype: str, round_intermediates: bool = False) -> np.ndarray:
+    """Y = GELU(X + bias) + R (exact erf GELU) in fp64, [rows, H]; with
+    round_intermediates, X + bias and its GELU are rounded to the dtype first
+    (the unfused chain that stores them)."""
     xs, rs = _raw(x, dtype), _raw(r, dtype)
     assert xs.shape == rs.shape and xs.ndim == 2
     rows, H = xs.shape
@@ -155,5 +158,6 @@ def oracle_bias_gelu_residual(x, r, bias, dtype: str) -> np.ndarray:
     assert b.shape == (H,)
     y = np.empty((rows, H), dtype=np.float64)
     _check(load().oracle_bias_gelu_residual(_ptr(xs), _ptr(rs), _DT[dtype], _ptr(b), rows, H,
-                                            _ptr(y)), "oracle_bias_gelu_residual")
+                                            int(round_intermediates), _ptr(y)),
+           "oracle_bias_gelu_residual")
     return y

@@ -103,3 +103,20 @@ def assert_softmax(y_gpu, y_ref, dtype, what=""):
         raise AssertionError(
             f"{what}: {int(bad.sum())} of {bad.size} softmax outputs out of bound; first "
             + ", ".join(f"{tuple(i)} gpu={yg[tuple(i)]!r} ref={y_ref[tuple(i)]!r}" for i in idx))
+
+
+def bgr_violations(y_gpu, y_ref, v_ref, r_ref, dtype: str, chain: bool = False) -> np.ndarray:
+    """Bias + GELU + residual bound, from the fp32 arithmetic (erff within
+    2 ulp): |dy| <= 1e-6 (1 + |x + bias| + |r|), plus one unit in the last place
+    of the exact value for 16-bit outputs.  The unfused chain (chain=True)
+    rounds X + bias and GELU of it to the dtype between kernels and may land a
+    unit away at each step: four units of the dtype at that scale."""
+    yg = to_f64(y_gpu)
+    scale = 1.0 + np.abs(v_ref) + np.abs(r_ref)
+    if dtype == "fp32":
+        bound = 1e-6 * scale
+    elif chain:
+        bound = 4 * ulp(scale, dtype)
+    else:
+        bound = 1e-6 * scale + ulp(y_ref, dtype)
+    return ~(np.abs(yg - y_ref) <= bound)

@@ -43,7 +43,8 @@ def header_defines():
 
 def test_header_declares_the_expected_entry_points():
     assert header_functions() == sorted([
-        "add_layernorm_fwd", "add_fwd", "layernorm_fwd", "softmax_fwd", "addln_strerror",
+        "add_layernorm_fwd", "add_fwd", "layernorm_fwd", "softmax_fwd", "bias_gelu_residual_fwd",
+        "bias_add_fwd", "gelu_fwd", "addln_strerror",
         "addln_max_hidden",
         "addln_get_device_error", "addln_set_force_path", "addln_set_wait_limit_ns",
         "addln_set_grid_cap", "addln_set_pdl", "addln_set_cta_shape", "addln_last_path",
@@ -170,6 +171,18 @@ def test_alias_rules(lib):
     assert lib.softmax_fwd(x, y, rows, H, 4, None) == b.ERR_DTYPE
     assert lib.softmax_fwd(x, y, rows, 32769, 1, None) == b.ERR_SHAPE
     assert lib.softmax_fwd(None, None, 0, H, 0, None) == b.OK
+    # bias + GELU + residual and its chain
+    bias = BASE + 0x2000000
+    assert lib.bias_gelu_residual_fwd(x, x + 0x1000000, bias, x + 8, rows, H, 0, None) == b.ERR_ALIAS
+    assert lib.bias_gelu_residual_fwd(x, x + 0x1000000, bias, bias, rows, H, 0, None) == b.ERR_ALIAS
+    assert lib.bias_gelu_residual_fwd(x, None, bias, y, rows, H, 0, None) == b.ERR_NULL
+    assert lib.bias_gelu_residual_fwd(x, x, bias, y, rows, 0, 0, None) == b.ERR_SHAPE
+    assert lib.bias_gelu_residual_fwd(x, x, bias, y, rows, H, 7, None) == b.ERR_DTYPE
+    assert lib.bias_gelu_residual_fwd(None, None, None, None, 0, H, 0, None) == b.OK
+    assert lib.bias_add_fwd(x, None, y, rows, H, 0, None) == b.ERR_NULL
+    assert lib.bias_add_fwd(x, bias, x + 4, rows, H, 0, None) == b.ERR_ALIAS
+    assert lib.gelu_fwd(x, x + 4, 64, 0, None) == b.ERR_ALIAS
+    assert lib.gelu_fwd(x, y, -1, 0, None) == b.ERR_SHAPE
 
 
 def test_missing_library_fails_loudly(tmp_path):

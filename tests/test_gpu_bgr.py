@@ -1,0 +1,89 @@
+"""GPU parity of the fused bias + GELU + residual kernel (and of the
+three-kernel chain it replaces) against the fp64 oracle on the same seeded
+inputs: vector and element paths, ragged and misaligned buffers, in place,
+and the full-size workloads on sampled rows."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _parity import bgr_violations
+
+pytestmark = pytest.mark.gpu
+mba = pytest.importorskip("memory_bound_add_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from memory_bound_add_gb300.build import build
+    build()
+
+
+def check(d, dtype, y, what, chain=False, rows=None):
+    x, r, b = d["x"], d["r"], d["beta"]
+    if rows is not None:
+        x, r, y = x[rows], r[rows], y[rows]
+    ref = oracle.oracle_bias_gelu_residual(x, r, b, dtype, round_intermediates=chain)
+    v = x.double().numpy() + b.double().numpy()
+    bad = bgr_violations(y, ref, v, r.double().numpy(), dtype, chain=chain)
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} outputs out of bound; first {i}: "
+                             f"gpu={y.double().numpy()[i]!r} ref={ref[i]!r}")
+
+
+@pytest.mark.parametrize("name", synth.BGR_NAMES)
+def test_small(name):
+    w = synth.with_rows(synth.get(name), 37)
+    d = synth.make_inputs(w, seed=1)
+    x, r, b = d["x"].cuda(), d["r"].cuda(), d["beta"].cuda()
+    y = mba.bias_gelu_residual(x, r, b)
+    torch.cuda.synchronize()
+    check(d, w.dtype, y.cpu(), name)
+    yu = mba.bias_gelu_residual_unfused(x, r, b)
+    torch.cuda.synchronize()
+    check(d, w.dtype, yu.cpu(), name + " unfused", chain=True)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+@pytest.mark.parametrize("H", [1, 3, 8, 1000, 1024, 4097])
+def test_shapes_misaligned_and_in_place(dtype, H):
+    w = synth.custom(9, H, dtype, r_dist=(0.0, 0.5), op="bias_gelu_residual")
+    d = synth.make_inputs(w, seed=H)
+    td = synth.TORCH_DTYPES[dtype]
+    x, r, b = d["x"].cuda(), d["r"].cuda(), d["beta"].cuda()
+    y = mba.bias_gelu_residual(x, r, b)
+    torch.cuda.synchronize()
+    check(d, dtype, y.cpu(), f"9x{H}")
+    n = 9 * H
+    xb = torch.empty(n + 8, dtype=td, device="cuda")
+    xm = xb[1:1 + n].view(9, H)
+    xm.copy_(x)
+    ym = torch.empty_like(xm)
+    mba.bias_gelu_residual_fwd(xm, r, b, ym)
+    torch.cuda.synchronize()
+    check(d, dtype, ym.cpu(), f"9x{H} misaligned")
+    xi = x.clone()
+    mba.bias_gelu_residual_fwd(xi, r, b, xi)            # y = x in place
+    ri = r.clone()
+    mba.bias_gelu_residual_fwd(x, ri, b, ri)            # y = r in place
+    torch.cuda.synchronize()
+    check(d, dtype, xi.cpu(), f"9x{H} y=x")
+    check(d, dtype, ri.cpu(), f"9x{H} y=r")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", synth.BGR_NAMES)
+def test_full_size_sampled_rows(name):
+    w = synth.get(name)
+    d = synth.make_inputs(w, seed=0)
+    y = mba.bias_gelu_residual(d["x"].cuda(), d["r"].cuda(), d["beta"].cuda()).cpu()
+    g = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([np.arange(8), np.arange(w.rows - 8, w.rows),
+                                     g.choice(w.rows, size=min(64, w.rows), replace=False)]))
+    check(d, w.dtype, y, f"{name} full size", rows=rows)

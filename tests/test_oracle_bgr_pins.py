@@ -120,3 +120,16 @@ def test_diagram_numbers_and_the_corrected_accounting():
     assert w.algorithmic_bytes() - 4 * w.H == 3 * t * MB          # 24 MB, not 16
     # ... against 7 tensor passes unfused (56 MB, not 48): R is a second input
     assert (2 + 2 + 3) * t == 56
+
+
+def test_round_intermediates_is_the_stored_chain():
+    # the chain mode equals rounding by hand between the steps (oracle_round)
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(4, 32, generator=g).to(torch.bfloat16)
+    r = torch.randn(4, 32, generator=g).to(torch.bfloat16)
+    bias = 0.3 * torch.randn(32, generator=g)
+    y = oracle.oracle_bias_gelu_residual(x, r, bias, "bf16", round_intermediates=True)
+    v = oracle.oracle_round(x.double().numpy() + bias.double().numpy(), "bf16")
+    gl = oracle.oracle_round(np.vectorize(lambda t: 0.5 * t * (1 + math.erf(t / math.sqrt(2))))(v), "bf16")
+    assert np.array_equal(y, gl + r.double().numpy())
+    assert not np.array_equal(y, oracle.oracle_bias_gelu_residual(x, r, bias, "bf16"))
