@@ -75,6 +75,8 @@ def parse_args():
     ap.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch (1/0)")
     ap.add_argument("--cta-threads", type=int, default=0, help="TMA kernel threads per CTA (tuning)")
     ap.add_argument("--stages", type=int, default=0, help="TMA kernel staged rows per CTA (tuning)")
+    ap.add_argument("--chain", type=int, default=0,
+                    help="L > 0: time L dependent Add+LayerNorm layers per step (launch overhead study)")
     ap.add_argument("--kernel", choices=["fused", "add"], default="fused",
                     help="add: time the unfused add kernel alone (same bytes as Y-only fused)")
     ap.add_argument("--only-fused", action="store_true",
@@ -651,10 +653,87 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_chain(args):
+    """L dependent layers per step: x_{l+1} = LayerNorm(x_l + R).  Timed as
+    eager launches, as a CUDA graph, and as a CUDA graph with programmatic
+    dependent launch, to measure what launching costs on this GPU against
+    the pages' 3-10 us per launch ("算子融合的收益量化" section 2)."""
+    import memory_bound_add_gb300 as mba
+    from memory_bound_add_gb300.build import build
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build()
+    w = synth.get(args.config)
+    if args.rows:
+        w = synth.with_rows(w, args.rows)
+    if w.op != "add_layernorm":
+        raise SystemExit("--chain runs the Add+LayerNorm workloads")
+    d = synth.make_inputs(w, seed=args.seed)
+    L = args.chain
+    x0, r = d["x"].to(dev), d["r"].to(dev)
+    g, b = d["gamma"].to(dev), d["beta"].to(dev)
+    bufs = [torch.empty_like(x0), torch.empty_like(x0)]
+
+    def step():
+        x = x0
+        for l in range(L):
+            y = bufs[l & 1]
+            mba.add_layernorm_fwd(x, r, g, b, y, eps=d["eps"])
+            x = y
+
+    K = args.steps or 200
+    W = max(3, args.warmup)
+    stream = torch.cuda.current_stream()
+    out = {}
+    for pdl in (0, 1):
+        mba.addln_set_pdl(pdl)
+        for _ in range(W):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        eager = e0.elapsed_time(e1) / 1e3 / (K * L)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(W):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(K):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        graphed = e0.elapsed_time(e1) / 1e3 / (K * L)
+        out[f"eager_pdl{pdl}_us_per_layer"] = round(eager * 1e6, 3)
+        out[f"graph_pdl{pdl}_us_per_layer"] = round(graphed * 1e6, 3)
+    mba.addln_set_pdl(1)
+    best = min(out[k] for k in out) / 1e6
+    alg = w.algorithmic_bytes()
+    print(json.dumps({
+        "metric": METRIC + " (dependent layer chain)", "value": round(alg / best / 1e9, 2),
+        "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W,
+        "ms_per_step": round(best * L * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "layers_per_step": L, "rows": w.rows, "H": w.H,
+                   "io_dtype": w.dtype, "l2": "one layer's working set; no rotation (a chain "
+                   "reads what the previous layer wrote, as a model does)"},
+        "chain": out, "gpu_launches": K * L,
+    }), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.chain > 0:
+        run_chain(args)
     else:
         run_ours(args)
 

@@ -124,8 +124,9 @@ int softmax_fwd(const void *x, void *y, int64_t rows, int64_t H, int dtype, void
  *   x, r  [rows, H] inputs in dtype (required)
  *   bias  [H] fp32 (required)
  *   y     [rows, H] output in dtype; may be x or r exactly (in place)
- * fp32 arithmetic with CUDA's erff; Y rounded to nearest even.  One read of X
- * and R, one write of Y.  Same conventions and error codes as the calls above.
+ * fp32 arithmetic; erf by Abramowitz and Stegun's formula 7.1.26 (absolute
+ * error below 1.5e-7); Y rounded to nearest even.  One read of X and R, one
+ * write of Y.  Same conventions and error codes as the calls above.
  */
 int bias_gelu_residual_fwd(const void *x, const void *r, const float *bias, void *y,
                            int64_t rows, int64_t H, int dtype, void *stream);

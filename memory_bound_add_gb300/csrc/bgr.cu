@@ -1,8 +1,9 @@
 // Bias + GELU + residual, fused: Y = GELU(X + bias) + R, one read of X and R
 // and one write of Y -- the single fused kernel of the BiasAdd -> GELU ->
 // Residual diagram in "算子融合的收益量化".  GELU is the exact form
-// v * Phi(v) = v/2 * (1 + erf(v / sqrt 2)) with CUDA's erff.  bias is fp32
-// [H], broadcast along rows.
+// v * Phi(v) = v/2 * (1 + erf(v / sqrt 2)), erf by the published rational
+// approximation below (absolute error below 1.5e-7).  bias is fp32 [H],
+// broadcast along rows.
 //
 // Also the two extra steps of the diagram's unfused chain, each its own
 // kernel with its own HBM round trip: T = X + bias and U = GELU(T) (the third
@@ -20,8 +21,22 @@ namespace ew {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
+// GELU(v) = v/2 * (1 + erf(v / sqrt 2)).  erf from Abramowitz and Stegun,
+// Handbook of Mathematical Functions (1964), formula 7.1.26 (after Hastings):
+// for a >= 0, erfc(a) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) e^(-a^2)
+// with t = 1 / (1 + p a), |error| <= 1.5e-7.  With z = v / sqrt 2 and
+// a = |z|, 1 + erf(z) is erfc(a) for z < 0 (no cancellation on the negative
+// side) and 2 - erfc(a) for z >= 0.  One fast reciprocal, one hardware
+// exponential and a degree-5 Horner polynomial.
 __device__ __forceinline__ float gelu(float v) {
-  return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+  constexpr float p = 0.3275911f;
+  constexpr float a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f,
+                  a4 = -1.453152027f, a5 = 1.061405429f;
+  const float a = fabsf(v) * 0.70710678118654752f;
+  const float t = __fdividef(1.0f, fmaf(p, a, 1.0f));
+  const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, a5, a4), a3), a2), a1);
+  const float erfc_a = poly * __expf(-a * a);
+  return 0.5f * v * (v >= 0.f ? 2.0f - erfc_a : erfc_a);
 }
 
 // What each element becomes.  kBgr: GELU(x + b) + r; kBias: x + b; kGelu: GELU(x).
@@ -49,8 +64,24 @@ __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* 
   pdl_trigger();
   pdl_wait();
   const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads * kUnroll;
-  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kThreads * kUnroll + threadIdx.x; i0 < nvec;
-       i0 += step) {
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kThreads * kUnroll + threadIdx.x;
+  // bias column of vector i is i % hvec; advanced incrementally (one add and
+  // at most one subtraction a vector) instead of a 64-bit remainder each time
+  const int64_t tmod = kThreads % hvec, smod = step % hvec;
+  int64_t col0 = HAS_B ? first % hvec : 0;
+  for (int64_t i0 = first; i0 < nvec; i0 += step) {
+    int64_t cols[kUnroll];
+    if constexpr (HAS_B) {
+      int64_t cc = col0;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        cols[u] = cc;
+        cc += tmod;
+        if (cc >= hvec) cc -= hvec;
+      }
+      col0 += smod;
+      if (col0 >= hvec) col0 -= hvec;
+    }
     uint4 xs[kUnroll], rs[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -68,7 +99,7 @@ __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* 
         IO::unpack(xs[u], f);
         if constexpr (HAS_R) IO::unpack(rs[u], g);
         if constexpr (HAS_B) {
-          const float* bp = bias + (i % hvec) * VEC;
+          const float* bp = bias + cols[u] * VEC;
 #pragma unroll
           for (int q = 0; q < VEC / 4; ++q) {
             const float4 t = ld_param_f4(bp + 4 * q);
