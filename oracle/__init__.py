@@ -18,5 +18,6 @@ from .oracle import (
     oracle_add_layernorm,
     oracle_softmax,
     oracle_bias_gelu_residual,
+    oracle_add_layernorm_bwd,
     load,
 )

@@ -41,6 +41,15 @@
  *   Y_ij = GELU(v_ij) + r_ij,   GELU(v) = v * Phi(v) = v/2 * (1 + erf(v / sqrt 2))
  * (the exact, erf form; the page names no variant), fp64 with libm erf.
  *
+ * Backward of the fused operation (the pages give no backward: this is the
+ * textbook derivative of the definition above).  Inputs: dY, the stored sum A,
+ * the per-row mean and rstd as saved, gamma, and optionally dA_in, a gradient
+ * reaching A from elsewhere (A is also the residual stream).  Per row:
+ *   xhat_j = (A_j - mean) * rstd,   g_j = dY_j * gamma_j
+ *   dA_j   = rstd * (g_j - (1/H) sum_k g_k - xhat_j (1/H) sum_k g_k xhat_k) + dA_in_j
+ *   dX = dR = dA
+ * and over rows:  dgamma_j = sum_i dY_ij xhat_ij,  dbeta_j = sum_i dY_ij.
+ *
  * dtype codes: 0 = IEEE binary32, 1 = IEEE binary16, 2 = bfloat16.
  * Return value: 0 on success, -1 on a bad argument.
  *
@@ -292,5 +301,58 @@ int oracle_bias_gelu_residual(const void *x, const void *r, int dtype, const flo
                 g = round_to_dtype(g, dtype);
             y[k] = g + decode_at(r, dtype, k);
         }
+    return 0;
+}
+
+/* Backward; dy, a, dres in dtype ([rows, H]); mean, rstd fp32 [rows]; gamma
+ * fp32 [H]; dres may be NULL.  Outputs fp64: dx [rows, H], dgamma, dbeta [H]
+ * (each output may be NULL). */
+int oracle_add_layernorm_bwd(const void *dy, const void *a, const float *mean, const float *rstd,
+                             const float *gamma, const void *dres, int dtype, int64_t rows,
+                             int64_t H, double *dx, double *dgamma, double *dbeta)
+{
+    if (bad_dtype(dtype) || rows < 0 || H <= 0)
+        return -1;
+    if (rows > 0 && (!dy || !a || !mean || !rstd || !gamma))
+        return -1;
+    double *xhat = (double *)malloc((size_t)H * sizeof(double));
+    double *g = (double *)malloc((size_t)H * sizeof(double));
+    if (!xhat || !g) {
+        free(xhat);
+        free(g);
+        return -1;
+    }
+    if (dgamma)
+        for (int64_t j = 0; j < H; ++j)
+            dgamma[j] = 0.0;
+    if (dbeta)
+        for (int64_t j = 0; j < H; ++j)
+            dbeta[j] = 0.0;
+    for (int64_t i = 0; i < rows; ++i) {
+        const double mu = (double)mean[i], rs = (double)rstd[i];
+        double sg = 0.0, sgx = 0.0;
+        for (int64_t j = 0; j < H; ++j) {
+            const int64_t k = i * H + j;
+            const double dyk = decode_at(dy, dtype, k);
+            xhat[j] = (decode_at(a, dtype, k) - mu) * rs;
+            g[j] = dyk * (double)gamma[j];
+            sg += g[j];
+            sgx += g[j] * xhat[j];
+            if (dgamma)
+                dgamma[j] += dyk * xhat[j];
+            if (dbeta)
+                dbeta[j] += dyk;
+        }
+        const double mg = sg / (double)H, mgx = sgx / (double)H;
+        if (dx)
+            for (int64_t j = 0; j < H; ++j) {
+                double d = rs * (g[j] - mg - xhat[j] * mgx);
+                if (dres)
+                    d += decode_at(dres, dtype, i * H + j);
+                dx[i * H + j] = d;
+            }
+    }
+    free(xhat);
+    free(g);
     return 0;
 }

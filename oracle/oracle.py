@@ -37,8 +37,11 @@ def load():
             lib.oracle_softmax.argtypes = [_P, ctypes.c_int, _I64, _I64, _P, _P, _P]
             lib.oracle_bias_gelu_residual.argtypes = [_P, _P, ctypes.c_int, _P, _I64, _I64,
                                                       ctypes.c_int, _P]
+            lib.oracle_add_layernorm_bwd.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_int, _I64,
+                                                     _I64, _P, _P, _P]
             for f in ("oracle_decode", "oracle_round", "oracle_add", "oracle_layernorm",
-                      "oracle_add_layernorm", "oracle_softmax", "oracle_bias_gelu_residual"):
+                      "oracle_add_layernorm", "oracle_softmax", "oracle_bias_gelu_residual",
+                      "oracle_add_layernorm_bwd"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -161,3 +164,22 @@ def oracle_bias_gelu_residual(x, r, bias, dtype: str, round_intermediates: bool 
                                             int(round_intermediates), _ptr(y)),
            "oracle_bias_gelu_residual")
     return y
+
+
+def oracle_add_layernorm_bwd(dy, a, mean, rstd, gamma, dtype: str, dres=None) -> dict:
+    """Backward of the fused operation (textbook derivative) in fp64: dx
+    ([rows, H], = dX = dR), dgamma, dbeta ([H]).  a is the stored sum A in the
+    dtype; mean, rstd are the saved fp32 statistics."""
+    dys, As = _raw(dy, dtype), _raw(a, dtype)
+    assert dys.shape == As.shape and dys.ndim == 2
+    rows, H = dys.shape
+    m, rs, g = _f32(mean), _f32(rstd), _f32(gamma)
+    assert m.shape == (rows,) and rs.shape == (rows,) and g.shape == (H,)
+    dr = _raw(dres, dtype) if dres is not None else None
+    dx = np.empty((rows, H), dtype=np.float64)
+    dg = np.empty(H, dtype=np.float64)
+    db = np.empty(H, dtype=np.float64)
+    _check(load().oracle_add_layernorm_bwd(_ptr(dys), _ptr(As), _ptr(m), _ptr(rs), _ptr(g),
+                                           _ptr(dr), _DT[dtype], rows, H, _ptr(dx), _ptr(dg),
+                                           _ptr(db)), "oracle_add_layernorm_bwd")
+    return {"dx": dx, "dgamma": dg, "dbeta": db}

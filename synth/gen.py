@@ -91,3 +91,12 @@ def make_affine(H: int, seed: int = 0) -> tuple:
     gamma = (np.float32(1.0) + np.float32(0.1) * gg.standard_normal(H, dtype=np.float32)).astype(np.float32)
     beta = (np.float32(0.1) * gb.standard_normal(H, dtype=np.float32)).astype(np.float32)
     return torch.from_numpy(gamma), torch.from_numpy(beta)
+
+
+def make_grad(w: Workload, seed: int = 0, scale: float = 1.0):
+    """Upstream gradient dY ~ N(0, scale) for workload w, rounded to its dtype
+    (child stream 6 of SeedSequence(seed); streams 0-5 are make_inputs')."""
+    ss = np.random.SeedSequence(seed)
+    gd = np.random.Generator(np.random.PCG64(ss.spawn(7)[6]))
+    v = _normal_f32(gd, w.rows * w.H, 0.0, scale)
+    return torch.from_numpy(v).view(w.rows, w.H).to(TORCH_DTYPES[w.dtype]).contiguous()
