@@ -67,6 +67,7 @@ extern "C" {
 #define ADDLN_ERR_UNSUPPORTED (-7)    /* a forced kernel path cannot run these arguments */
 #define ADDLN_ERR_DEVICE_TIMEOUT (-8) /* a kernel's bounded wait on its own copy ran out */
 #define ADDLN_ERR_CUDA (-9)           /* a CUDA runtime call outside a launch failed */
+#define ADDLN_ERR_WORKSPACE (-10)     /* workspace missing, too small or not 16-byte aligned */
 
 /* kernel paths for addln_set_force_path */
 #define ADDLN_PATH_AUTO 0
@@ -140,6 +141,39 @@ int bias_add_fwd(const void *x, const float *bias, void *t, int64_t rows, int64_
  * contiguous elements; u may be t exactly.  Step 3 (Residual) is add_fwd. */
 int gelu_fwd(const void *t, void *u, int64_t n, int dtype, void *stream);
 
+/*
+ * Backward of add_layernorm_fwd.  The pages give no backward (fusion of
+ * automatic differentiation is only named as a direction in "CUDA算子融合优化"
+ * section 5); this is the textbook derivative of the definition above.  Per row
+ * i, with xhat = (A - mean) * rstd and g = dY * gamma:
+ *     dA = rstd * (g - (1/H) sum_j g - xhat * (1/H) sum_j g xhat) + dA_in
+ *     dX = dR = dA                              (written once, to dx)
+ * and over all rows dgamma = sum_i dY xhat, dbeta = sum_i dY.
+ *   dy         [rows, H] upstream gradient in dtype (required)
+ *   a          [rows, H] the stored sum A (resid_out of the forward), dtype
+ *   mean, rstd [rows] fp32, as saved by the forward
+ *   gamma      [H] fp32
+ *   dres       [rows, H] gradient reaching A from elsewhere (A is also the
+ *              residual stream), or NULL
+ *   dx         [rows, H] output in dtype; may be dy, a or dres exactly
+ *   dgamma, dbeta [H] fp32 outputs, both or neither (NULL: not computed)
+ *   workspace  device scratch of at least add_layernorm_bwd_workspace_size()
+ *              bytes, 16-byte aligned, owned by the caller; needed only with
+ *              dgamma / dbeta.  Holds per-CTA column partials, summed in a
+ *              fixed order, so the results are bitwise reproducible.
+ * rows == 0 zero-fills dgamma and dbeta.  fp32 arithmetic; dx rounded to
+ * nearest even.  Returns ADDLN_OK, or a negative code (ADDLN_ERR_WORKSPACE
+ * for a missing, short or misaligned workspace).
+ */
+int add_layernorm_bwd(const void *dy, const void *a, const float *mean, const float *rstd,
+                      const float *gamma, const void *dres, void *dx, float *dgamma, float *dbeta,
+                      int64_t rows, int64_t H, int dtype, void *workspace, int64_t workspace_bytes,
+                      void *stream);
+
+/* Bytes of workspace add_layernorm_bwd needs for rows x H in dtype on the
+ * current device (0 when rows == 0), or a negative code. */
+int64_t add_layernorm_bwd_workspace_size(int64_t rows, int64_t H, int dtype);
+
 /* Static text for a return code (never NULL). */
 const char *addln_strerror(int code);
 
@@ -149,7 +183,7 @@ int64_t addln_max_hidden(int dtype);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error
- * words, which a kernel (add-LayerNorm or softmax) sets when a bounded wait
+ * words, which a kernel (add-LayerNorm, softmax or backward) sets when a bounded wait
  * on its own TMA copy runs out.
  * Returns ADDLN_OK, ADDLN_ERR_DEVICE_TIMEOUT, or ADDLN_ERR_CUDA if the
  * synchronisation or the read failed.  Rows of a kernel that timed out are

@@ -17,6 +17,9 @@ from .binding import (  # noqa: F401
     gelu_fwd,
     bias_gelu_residual,
     bias_gelu_residual_unfused,
+    add_layernorm_bwd,
+    add_layernorm_bwd_workspace_size,
+    add_layernorm_backward,
     addln_get_device_error,
     addln_set_force_path,
     addln_set_wait_limit_ns,

@@ -23,6 +23,7 @@ DTYPE_CODE = {torch.float32: FP32, torch.float16: FP16, torch.bfloat16: BF16}
 OK = 0
 ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_EPS, ERR_ALIAS = -1, -2, -3, -4, -5
 ERR_LAUNCH, ERR_UNSUPPORTED, ERR_DEVICE_TIMEOUT, ERR_CUDA = -6, -7, -8, -9
+ERR_WORKSPACE = -10
 
 PATH_AUTO, PATH_WARP_VEC, PATH_CTA_TMA, PATH_CTA_VEC, PATH_SCALAR = 0, 1, 2, 3, 4
 
@@ -39,6 +40,9 @@ SIGNATURES = {
     "bias_gelu_residual_fwd": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, ctypes.c_int, _P]),
     "bias_add_fwd": (ctypes.c_int, [_P, _P, _P, _I64, _I64, ctypes.c_int, _P]),
     "gelu_fwd": (ctypes.c_int, [_P, _P, _I64, ctypes.c_int, _P]),
+    "add_layernorm_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                                         ctypes.c_int, _P, _I64, _P]),
+    "add_layernorm_bwd_workspace_size": (ctypes.c_int64, [_I64, _I64, ctypes.c_int]),
     "addln_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "addln_max_hidden": (ctypes.c_int64, [ctypes.c_int]),
     "addln_get_device_error": (ctypes.c_int, [_P]),
@@ -257,6 +261,44 @@ def bias_gelu_residual_unfused(x, r, bias, t=None, y=None, stream=None):
     gelu_fwd(t, t, stream=stream)
     add_fwd(t, r, y, stream=stream)
     return y
+
+
+def add_layernorm_bwd_workspace_size(rows: int, H: int, dtype: int) -> int:
+    n = int(lib().add_layernorm_bwd_workspace_size(int(rows), int(H), int(dtype)))
+    if n < 0:
+        raise AddLNError(n, "add_layernorm_bwd_workspace_size")
+    return n
+
+
+def add_layernorm_bwd(dy, a, mean, rstd, gamma, dx, dgamma=None, dbeta=None, dres=None,
+                      workspace=None, stream=None):
+    """Backward of add_layernorm_fwd into caller-provided dx (and dgamma,
+    dbeta).  workspace: a CUDA tensor of at least
+    add_layernorm_bwd_workspace_size(rows, H, dtype) bytes (allocated here
+    with PyTorch when None and dgamma is wanted)."""
+    rows, H = _rows_shape(dy)
+    _require(dy, "dy")
+    for t, n in ((a, "a"), (dx, "dx"), (dres, "dres")):
+        if t is not None:
+            _require(t, n, dy.dtype, like=dy)
+    dt = DTYPE_CODE[dy.dtype]
+    if dgamma is not None and workspace is None:
+        nbytes = add_layernorm_bwd_workspace_size(rows, H, dt)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dy.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().add_layernorm_bwd(_ptr(dy), _ptr(a), _ptr(mean), _ptr(rstd), _ptr(gamma),
+                                   _ptr(dres), _ptr(dx), _ptr(dgamma), _ptr(dbeta), rows, H, dt,
+                                   _ptr(workspace), wbytes, _stream(stream)), "add_layernorm_bwd")
+
+
+def add_layernorm_backward(dy, a, mean, rstd, gamma, dres=None, stream=None):
+    """Allocate outputs with PyTorch; returns (dx, dgamma, dbeta)."""
+    dx = torch.empty_like(dy)
+    H = dy.shape[-1]
+    dg = torch.empty(H, dtype=torch.float32, device=dy.device)
+    db = torch.empty(H, dtype=torch.float32, device=dy.device)
+    add_layernorm_bwd(dy, a, mean, rstd, gamma, dx, dg, db, dres=dres, stream=stream)
+    return dx, dg, db
 
 
 def addln_max_hidden(dtype: int) -> int:

@@ -309,6 +309,75 @@ int gelu_fwd(const void* x, void* u, int64_t n, int dtype, void* stream) {
   return addln::launch_gelu(dtype, x, u, n, c);
 }
 
+int64_t add_layernorm_bwd_workspace_size(int64_t rows, int64_t H, int dtype) {
+  if (!valid_dtype(dtype)) return ADDLN_ERR_DTYPE;
+  if (rows < 0 || H <= 0 || H > max_hidden(dtype) || rows > INT64_MAX / (H * 4))
+    return ADDLN_ERR_SHAPE;
+  if (rows == 0) return 0;
+  DeviceInfo dev;
+  const int rc = device_info(&dev);
+  if (rc != ADDLN_OK) return rc;
+  // the larger of the vector and the element plan: the pointers decide later
+  const int64_t v = addln::bwd_workspace_bytes(dtype, rows, H, true, dev);
+  const int64_t s = addln::bwd_workspace_bytes(dtype, rows, H, false, dev);
+  if (v < 0) return v;
+  if (s < 0) return s;
+  return v > s ? v : s;
+}
+
+int add_layernorm_bwd(const void* dy, const void* a, const float* mean, const float* rstd,
+                      const float* gamma, const void* dres, void* dx, float* dgamma, float* dbeta,
+                      int64_t rows, int64_t H, int dtype, void* workspace,
+                      int64_t workspace_bytes, void* stream) {
+  if (!valid_dtype(dtype)) return ADDLN_ERR_DTYPE;
+  if (rows < 0 || H <= 0 || H > max_hidden(dtype) || rows > INT64_MAX / (H * 4))
+    return ADDLN_ERR_SHAPE;
+  if ((dgamma == nullptr) != (dbeta == nullptr)) return ADDLN_ERR_NULL;
+  if (workspace_bytes < 0) return ADDLN_ERR_WORKSPACE;
+  if (rows == 0) {
+    if (dgamma == nullptr) return ADDLN_OK;
+    if (cudaMemsetAsync(dgamma, 0, H * 4, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+        cudaMemsetAsync(dbeta, 0, H * 4, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return ADDLN_ERR_CUDA;
+    return ADDLN_OK;
+  }
+  if (!dy || !a || !mean || !rstd || !gamma || !dx) return ADDLN_ERR_NULL;
+  const int64_t tb = rows * H * elem_bytes(dtype);
+  const Range rdx = range_of(dx, tb);
+  const Range ins[6] = {range_of(dy, tb), range_of(a, tb), range_of(dres, tb),
+                        range_of(mean, rows * 4), range_of(rstd, rows * 4), range_of(gamma, H * 4)};
+  for (int i = 0; i < 6; ++i)
+    if (bad_pair(rdx, ins[i], i < 3)) return ADDLN_ERR_ALIAS;
+  const Range rg = range_of(dgamma, H * 4), rb = range_of(dbeta, H * 4);
+  const Range rw = range_of(dgamma ? workspace : nullptr, workspace_bytes);
+  const Range outs[4] = {rdx, rg, rb, rw};
+  for (int i = 1; i < 4; ++i) {
+    for (int k = 0; k < 6; ++k)
+      if (overlap(outs[i], ins[k])) return ADDLN_ERR_ALIAS;
+    for (int j = 0; j < i; ++j)
+      if (overlap(outs[i], outs[j])) return ADDLN_ERR_ALIAS;
+  }
+  LaunchCtx c;
+  c.stream = stream;
+  c.grid_cap = 0;
+  c.pdl = g_pdl.load(std::memory_order_relaxed) != 0;
+  c.cta_threads = 0;
+  c.stages = 0;
+  const int rc = device_info(&c.dev);
+  if (rc != ADDLN_OK) return rc;
+  const int64_t row_bytes = H * elem_bytes(dtype);
+  bool vec_ok = row_bytes % 16 == 0 && aligned16(dy) && aligned16(a) && aligned16(dx) &&
+                (!dres || aligned16(dres)) && aligned16(gamma);
+  const int force = g_force_path.load(std::memory_order_relaxed);
+  if (force == ADDLN_PATH_SCALAR) vec_ok = false;
+  const char* name = "none";
+  const int out = addln::launch_bwd(dtype, dy, a, mean, rstd, gamma, dres, dx, dgamma, dbeta, rows,
+                                    H, vec_ok, workspace, workspace_bytes,
+                                    g_wait_limit_ns.load(std::memory_order_relaxed), c, &name);
+  if (out == ADDLN_OK) g_last_path = name;
+  return out;
+}
+
 int add_fwd(const void* x, const void* r, void* a, int64_t n, int dtype, void* stream) {
   if (!valid_dtype(dtype)) return ADDLN_ERR_DTYPE;
   if (n < 0 || n > INT64_MAX / 4) return ADDLN_ERR_SHAPE;
@@ -341,6 +410,7 @@ const char* addln_strerror(int code) {
     case ADDLN_ERR_UNSUPPORTED: return "the forced kernel path cannot run these arguments";
     case ADDLN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait on its own copy ran out";
     case ADDLN_ERR_CUDA: return "a CUDA runtime call failed";
+    case ADDLN_ERR_WORKSPACE: return "workspace missing, too small or not 16-byte aligned";
     default: return "unknown error code";
   }
 }
@@ -355,7 +425,10 @@ int addln_get_device_error(void* stream) {
   if (rc != ADDLN_OK) return rc;
   rc = addln::read_and_clear_softmax_error(&code_sm);
   if (rc != ADDLN_OK) return rc;
-  return code != 0 ? code : code_sm;
+  int code_bw = 0;
+  rc = addln::read_and_clear_bwd_error(&code_bw);
+  if (rc != ADDLN_OK) return rc;
+  return code != 0 ? code : (code_sm != 0 ? code_sm : code_bw);
 }
 
 int addln_set_force_path(int path) {

@@ -78,6 +78,16 @@ int launch_bias_add(int dtype, const void* x, const float* bias, void* y, int64_
                     const LaunchCtx& c);
 int launch_gelu(int dtype, const void* x, void* y, int64_t n, const LaunchCtx& c);
 
+// Backward of add+LayerNorm: bytes of workspace the launch needs (its grid's
+// [2][H] fp32 column partials), and the launch (row kernel, then the column
+// sums when dgamma/dbeta are wanted).
+int64_t bwd_workspace_bytes(int dtype, int64_t rows, int64_t H, bool vec_ok, const DeviceInfo& dev);
+int launch_bwd(int dtype, const void* dy, const void* a, const float* mean, const float* rstd,
+               const float* gamma, const void* dres, void* dx, float* dgamma, float* dbeta,
+               int64_t rows, int64_t H, bool vec_ok, void* ws, int64_t ws_bytes,
+               uint64_t wait_limit_ns, const LaunchCtx& c, const char** name);
+int read_and_clear_bwd_error(int* code);
+
 // Remembers the CUDA error behind the last ADDLN_ERR_LAUNCH / ADDLN_ERR_CUDA
 // on this host thread (an int cudaError_t; 0 = none).
 void note_cuda_error(int err);

@@ -121,3 +121,36 @@ def bgr_violations(y_gpu, y_ref, v_ref, r_ref, dtype: str, chain: bool = False) 
     else:
         bound = 1e-6 * scale + ulp(y_ref, dtype)
     return ~(np.abs(yg - y_ref) <= bound)
+
+
+def assert_bwd(out, ref, inputs, dtype, what=""):
+    """Backward bounds, from the fp32 arithmetic: dA element (i, j) within
+    1e-5 * rstd_i * (|g_ij| + mean_k |g_ik| + |xhat_ij| mean_k |g_ik xhat_ik|)
+    + 1e-6 |dA_in_ij| (+ one ulp of the exact value for 16-bit outputs);
+    dgamma_j within 1e-5 sum_i |dY_ij xhat_ij|, dbeta_j within 1e-5 sum_i |dY_ij|
+    (+ 1e-30)."""
+    dy, a, mean, rstd, gamma, dres = inputs
+    dyd = to_f64(dy)
+    xh = (to_f64(a) - np.asarray(mean, np.float64)[:, None]) * np.asarray(rstd, np.float64)[:, None]
+    g = dyd * to_f64(gamma)[None, :]
+    scale = np.asarray(rstd, np.float64)[:, None] * (
+        np.abs(g) + np.abs(g).mean(axis=1, keepdims=True)
+        + np.abs(xh) * np.abs(g * xh).mean(axis=1, keepdims=True))
+    bound = 1e-5 * scale + 1e-30
+    if dres is not None:
+        bound = bound + 1e-6 * np.abs(to_f64(dres))
+    if dtype != "fp32":
+        bound = bound + ulp(ref["dx"], dtype)
+    dx = to_f64(out[0])
+    bad = ~(np.abs(dx - ref["dx"]) <= bound)
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} dx out of bound; first {i}: "
+                             f"gpu={dx[i]!r} ref={ref['dx'][i]!r} bound={bound[i]!r}")
+    for k, s in (("dgamma", np.abs(dyd * xh).sum(axis=0)), ("dbeta", np.abs(dyd).sum(axis=0))):
+        got = to_f64(out[1] if k == "dgamma" else out[2])
+        badk = ~(np.abs(got - ref[k]) <= 1e-5 * s + 1e-30)
+        if badk.any():
+            j = int(np.argwhere(badk)[0][0])
+            raise AssertionError(f"{what}: {int(badk.sum())} {k} out of bound; first {j}: "
+                                 f"gpu={got[j]!r} ref={ref[k][j]!r}")

@@ -44,7 +44,8 @@ def header_defines():
 def test_header_declares_the_expected_entry_points():
     assert header_functions() == sorted([
         "add_layernorm_fwd", "add_fwd", "layernorm_fwd", "softmax_fwd", "bias_gelu_residual_fwd",
-        "bias_add_fwd", "gelu_fwd", "addln_strerror",
+        "bias_add_fwd", "gelu_fwd", "add_layernorm_bwd", "add_layernorm_bwd_workspace_size",
+        "addln_strerror",
         "addln_max_hidden",
         "addln_get_device_error", "addln_set_force_path", "addln_set_wait_limit_ns",
         "addln_set_grid_cap", "addln_set_pdl", "addln_set_cta_shape", "addln_last_path",
@@ -68,7 +69,7 @@ def test_binding_signatures_cover_the_header():
     assert (binding.FP32, binding.FP16, binding.BF16) == (d["ADDLN_FP32"], d["ADDLN_FP16"],
                                                           d["ADDLN_BF16"])
     for k in ("NULL", "SHAPE", "DTYPE", "EPS", "ALIAS", "LAUNCH", "UNSUPPORTED",
-              "DEVICE_TIMEOUT", "CUDA"):
+              "DEVICE_TIMEOUT", "CUDA", "WORKSPACE"):
         assert getattr(binding, "ERR_" + k) == d["ADDLN_ERR_" + k]
     for k in ("AUTO", "WARP_VEC", "CTA_TMA", "CTA_VEC", "SCALAR"):
         assert getattr(binding, "PATH_" + k) == d["ADDLN_PATH_" + k]
@@ -76,7 +77,7 @@ def test_binding_signatures_cover_the_header():
 
 def test_strerror_and_limits(lib):
     from memory_bound_add_gb300 import binding as b
-    for code in range(-9, 1):
+    for code in range(-10, 1):
         assert lib.addln_strerror(code)
     assert b"unknown" in lib.addln_strerror(-99)
     assert lib.addln_max_hidden(b.FP32) == 16384
@@ -183,6 +184,30 @@ def test_alias_rules(lib):
     assert lib.bias_add_fwd(x, bias, x + 4, rows, H, 0, None) == b.ERR_ALIAS
     assert lib.gelu_fwd(x, x + 4, 64, 0, None) == b.ERR_ALIAS
     assert lib.gelu_fwd(x, y, -1, 0, None) == b.ERR_SHAPE
+    # backward (fake pointers: every call fails its checks before CUDA)
+    dy, a, mu, rs, g = x, BASE + 0x1000000, BASE + 0x4000000, BASE + 0x4100000, BASE + 0x2000000
+    dx, dg, db, ws = BASE + 0x5000000, BASE + 0x6000000, BASE + 0x6100000, BASE + 0x7000000
+
+    def bwd(**kw):
+        args = dict(dy=dy, a=a, mu=mu, rs=rs, g=g, dres=None, dx=dx, dg=dg, db=db, rows=rows, H=H,
+                    dtype=0, ws=ws, wsb=1 << 20)
+        args.update(kw)
+        return lib.add_layernorm_bwd(args["dy"], args["a"], args["mu"], args["rs"], args["g"],
+                                     args["dres"], args["dx"], args["dg"], args["db"],
+                                     args["rows"], args["H"], args["dtype"], args["ws"],
+                                     args["wsb"], None)
+    assert bwd(dtype=5) == b.ERR_DTYPE
+    assert bwd(H=0) == b.ERR_SHAPE
+    assert bwd(db=None) == b.ERR_NULL                 # dgamma without dbeta
+    assert bwd(a=None) == b.ERR_NULL
+    assert bwd(wsb=-1) == b.ERR_WORKSPACE
+    assert bwd(dx=dy + 4) == b.ERR_ALIAS              # partial overlap with dY
+    assert bwd(dg=g) == b.ERR_ALIAS                   # dgamma over gamma
+    assert bwd(ws=dx) == b.ERR_ALIAS                  # workspace over dX
+    assert bwd(db=dg + 4) == b.ERR_ALIAS
+    assert lib.add_layernorm_bwd_workspace_size(4, 8, 9) == b.ERR_DTYPE
+    assert lib.add_layernorm_bwd_workspace_size(4, 0, 0) == b.ERR_SHAPE
+    assert lib.add_layernorm_bwd_workspace_size(0, 8, 0) == 0
 
 
 def test_missing_library_fails_loudly(tmp_path):
