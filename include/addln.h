@@ -174,6 +174,37 @@ int add_layernorm_bwd(const void *dy, const void *a, const float *mean, const fl
  * current device (0 when rows == 0), or a negative code. */
 int64_t add_layernorm_bwd_workspace_size(int64_t rows, int64_t H, int dtype);
 
+/* Size of the built-in scratch buffer add_layernorm_bwd_noalloc uses. */
+#define ADDLN_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * add_layernorm_bwd without a caller-provided workspace, for callers that
+ * cannot allocate device memory: e.g. a plugin that a framework or inference
+ * engine gives only tensor pointers (the host owns all device memory and
+ * offers no allocator), or a latency-critical loop where cudaMalloc/cudaFree
+ * are ruled out because they can block and synchronise.  The source pages
+ * have no counterpart: this is a deployment convenience, not part of the
+ * method.
+ *
+ * Same arguments, results and error codes as add_layernorm_bwd, minus the
+ * workspace.  The column partials go to a device buffer of
+ * ADDLN_NOALLOC_SCRATCH_BYTES (32 MiB) compiled into the library, which every
+ * GPU that loads the library keeps until the process exits.  No device memory
+ * is allocated by the call.  The first call on each device looks up the
+ * buffer's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  A shape whose partials need
+ * more than the buffer (add_layernorm_bwd_workspace_size() >
+ * ADDLN_NOALLOC_SCRATCH_BYTES) is rejected with ADDLN_ERR_WORKSPACE before any
+ * launch.  All calls on a device share the buffer, which keeps the last call's
+ * contents (nothing in it needs to start at zero): calls that may overlap on
+ * the GPU, from other streams or host threads, race on it and must be
+ * serialised by the caller.
+ */
+int add_layernorm_bwd_noalloc(const void *dy, const void *a, const float *mean,
+                              const float *rstd, const float *gamma, const void *dres, void *dx,
+                              float *dgamma, float *dbeta, int64_t rows, int64_t H, int dtype,
+                              void *stream);
+
 /* Static text for a return code (never NULL). */
 const char *addln_strerror(int code);
 

@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     add_layernorm_bwd,
     add_layernorm_bwd_workspace_size,
     add_layernorm_backward,
+    add_layernorm_bwd_noalloc,
     addln_get_device_error,
     addln_set_force_path,
     addln_set_wait_limit_ns,

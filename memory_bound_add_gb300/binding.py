@@ -43,6 +43,8 @@ SIGNATURES = {
     "add_layernorm_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
                                          ctypes.c_int, _P, _I64, _P]),
     "add_layernorm_bwd_workspace_size": (ctypes.c_int64, [_I64, _I64, ctypes.c_int]),
+    "add_layernorm_bwd_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                                                 ctypes.c_int, _P]),
     "addln_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "addln_max_hidden": (ctypes.c_int64, [ctypes.c_int]),
     "addln_get_device_error": (ctypes.c_int, [_P]),
@@ -289,6 +291,25 @@ def add_layernorm_bwd(dy, a, mean, rstd, gamma, dx, dgamma=None, dbeta=None, dre
     _check(lib().add_layernorm_bwd(_ptr(dy), _ptr(a), _ptr(mean), _ptr(rstd), _ptr(gamma),
                                    _ptr(dres), _ptr(dx), _ptr(dgamma), _ptr(dbeta), rows, H, dt,
                                    _ptr(workspace), wbytes, _stream(stream)), "add_layernorm_bwd")
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def add_layernorm_bwd_noalloc(dy, a, mean, rstd, gamma, dx, dgamma=None, dbeta=None, dres=None,
+                              stream=None):
+    """add_layernorm_bwd with the library's built-in scratch buffer instead of
+    a workspace, for callers that cannot allocate device memory.  Calls that
+    can overlap on the GPU share that buffer and must be serialised."""
+    rows, H = _rows_shape(dy)
+    _require(dy, "dy")
+    for t, n in ((a, "a"), (dx, "dx"), (dres, "dres")):
+        if t is not None:
+            _require(t, n, dy.dtype, like=dy)
+    _check(lib().add_layernorm_bwd_noalloc(_ptr(dy), _ptr(a), _ptr(mean), _ptr(rstd), _ptr(gamma),
+                                           _ptr(dres), _ptr(dx), _ptr(dgamma), _ptr(dbeta), rows,
+                                           H, DTYPE_CODE[dy.dtype], _stream(stream)),
+           "add_layernorm_bwd_noalloc")
 
 
 def add_layernorm_backward(dy, a, mean, rstd, gamma, dres=None, stream=None):

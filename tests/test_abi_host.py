@@ -45,6 +45,7 @@ def test_header_declares_the_expected_entry_points():
     assert header_functions() == sorted([
         "add_layernorm_fwd", "add_fwd", "layernorm_fwd", "softmax_fwd", "bias_gelu_residual_fwd",
         "bias_add_fwd", "gelu_fwd", "add_layernorm_bwd", "add_layernorm_bwd_workspace_size",
+        "add_layernorm_bwd_noalloc",
         "addln_strerror",
         "addln_max_hidden",
         "addln_get_device_error", "addln_set_force_path", "addln_set_wait_limit_ns",
