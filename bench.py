@@ -75,6 +75,8 @@ def parse_args():
     ap.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch (1/0)")
     ap.add_argument("--cta-threads", type=int, default=0, help="TMA kernel threads per CTA (tuning)")
     ap.add_argument("--stages", type=int, default=0, help="TMA kernel staged rows per CTA (tuning)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time add_layernorm_bwd on an Add+LayerNorm workload")
     ap.add_argument("--chain", type=int, default=0,
                     help="L > 0: time L dependent Add+LayerNorm layers per step (launch overhead study)")
     ap.add_argument("--kernel", choices=["fused", "add"], default="fused",
@@ -728,12 +730,94 @@ def run_chain(args):
     }), flush=True)
 
 
+def bwd_algorithmic_bytes(w) -> int:
+    """Read dY and A once, mean and rstd, gamma; write dX, dgamma, dbeta."""
+    s = w.elem_bytes
+    return 3 * w.rows * w.H * s + 8 * w.rows + 12 * w.H
+
+
+def run_backward(args):
+    """Backward of the fused operation on one batch per step (dY seeded; A,
+    mean and rstd from the forward kernel), timed like the forward."""
+    import memory_bound_add_gb300 as mba
+    from memory_bound_add_gb300.build import build
+
+    ws_, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build()
+    w = synth.get(args.config)
+    if args.rows:
+        w = synth.with_rows(w, args.rows)
+    if w.op != "add_layernorm":
+        raise SystemExit("--backward runs the Add+LayerNorm workloads")
+    d = synth.make_inputs(w, seed=args.seed)
+    gamma, beta = d["gamma"].to(dev), d["beta"].to(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_set = 3 * w.rows * w.H * w.elem_bytes
+    n_sets = max(2, math.ceil(3 * l2 / per_set))
+    wsb = mba.add_layernorm_bwd_workspace_size(w.rows, w.H, mba.binding.DTYPE_CODE[d["x"].dtype])
+    sets = []
+    x, r = d["x"].to(dev), d["r"].to(dev)
+    for i in range(n_sets):
+        a = torch.empty_like(x)
+        mean = torch.empty(w.rows, device=dev)
+        rstd = torch.empty(w.rows, device=dev)
+        mba.add_layernorm_fwd(x, r, gamma, beta, torch.empty_like(x), a, mean, rstd, eps=d["eps"])
+        sets.append({"dy": synth.make_grad(w, seed=args.seed + i).to(dev), "a": a, "mean": mean,
+                     "rstd": rstd, "dx": torch.empty_like(x),
+                     "dg": torch.empty(w.H, device=dev), "db": torch.empty(w.H, device=dev),
+                     "ws": torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)})
+    torch.cuda.synchronize()
+
+    def step(i):
+        s = sets[i]
+        mba.add_layernorm_bwd(s["dy"], s["a"], s["mean"], s["rstd"], gamma, s["dx"], s["dg"],
+                              s["db"], workspace=s["ws"])
+
+    step(0)
+    torch.cuda.synchronize()
+    path = mba.addln_last_path()
+    t = time.time()
+    for i in range(20):
+        step(i % n_sets)
+    torch.cuda.synchronize()
+    est = (time.time() - t) / 20
+    K = args.steps if args.steps else max(100, int(1.0 / max(est, 1e-6)))
+    W = max(3, args.warmup)
+    graph_steps = args.graph_steps or max(n_sets, min(K, 256))
+    elapsed, _, _ = timed_graph_run(step, K, W, n_sets, graph_steps, lambda: None)
+    if mba.addln_get_device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+    alg = bwd_algorithmic_bytes(w)
+    peak, peak_kind = measured_peak()
+    value = alg * K / elapsed / 1e9
+    print(json.dumps({
+        "metric": "Add+LayerNorm backward effective HBM GB/s and % of GB300 peak; rows/sec",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W,
+        "ms_per_step": round(elapsed / K * 1e3, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "rows": w.rows, "H": w.H, "io_dtype": w.dtype,
+                   "outputs": "dX, dgamma, dbeta", "kernel_path": path,
+                   "algorithmic_bytes_per_step": alg, "workspace_bytes": wsb,
+                   "l2": f"inputs rotate over {n_sets} buffer sets (>= 3x L2)"},
+        "rows_per_s": round(w.rows * K / elapsed, 1),
+        "pct_of_measured_peak": round(100 * value / peak, 2),
+        "gpu_launches": 2 * K,
+        "roofline": {"bound": "hbm", "achieved": round(value, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(value / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": None},
+    }), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
     elif args.chain > 0:
         run_chain(args)
+    elif args.backward:
+        run_backward(args)
     else:
         run_ours(args)
 

@@ -73,7 +73,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3) k_bwd_warp(const BwdArgs p) {
   const int H = p.H;
   const int nvec = H / VEC;
   const bool cols = p.ws != nullptr;
-  float* part = reinterpret_cast<float*>(smem) + warp * 2 * H;  // this warp: dgamma[H], dbeta[H]
+  // this warp's partials, lane-major so a warp's accesses hit 32 distinct
+  // banks: column (lane + 32 k) * VEC + i lives at slot (k * VEC + i) * 32 + lane
+  // of the dgamma half [0, 32 NV VEC) and of the dbeta half after it
+  constexpr int kHalf = 32 * NV * VEC;
+  float* part = reinterpret_cast<float*>(smem) + warp * 2 * kHalf;
 
   bool ok[NV];
 #pragma unroll
@@ -81,12 +85,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3) k_bwd_warp(const BwdArgs p) {
   if (cols)
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (ok[k])
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          part[(lane + 32 * k) * VEC + e] = 0.f;
-          part[H + (lane + 32 * k) * VEC + e] = 0.f;
-        }
+      for (int e = 0; e < VEC; ++e) {
+        part[(k * VEC + e) * 32 + lane] = 0.f;
+        part[kHalf + (k * VEC + e) * 32 + lane] = 0.f;
+      }
   pdl_trigger();
   pdl_wait();
 
@@ -125,8 +128,9 @@ __global__ void __launch_bounds__(kWarps * 32, 3) k_bwd_warp(const BwdArgs p) {
         if (cols)
 #pragma unroll
           for (int i = 0; i < VEC; ++i) {
-            part[c * VEC + i] = fmaf(d[i], xh[k][i], part[c * VEC + i]);
-            part[H + c * VEC + i] += d[i];
+            float* sl = part + (k * VEC + i) * 32 + lane;
+            sl[0] = fmaf(d[i], xh[k][i], sl[0]);
+            sl[kHalf] += d[i];
           }
       }
     }
@@ -156,9 +160,12 @@ __global__ void __launch_bounds__(kWarps * 32, 3) k_bwd_warp(const BwdArgs p) {
     const float* all = reinterpret_cast<const float*>(smem);
     float* out = p.ws + static_cast<int64_t>(blockIdx.x) * 2 * H;
     for (int j = tid; j < 2 * H; j += kWarps * 32) {
-      float s = all[j];
+      const int half = j < H ? 0 : 1, col = j - half * H;
+      const int c = col / VEC, i = col - c * VEC;
+      const int slot = half * kHalf + ((c >> 5) * VEC + i) * 32 + (c & 31);
+      float s = all[slot];
 #pragma unroll
-      for (int w = 1; w < kWarps; ++w) s += all[w * 2 * H + j];
+      for (int w = 1; w < kWarps; ++w) s += all[w * 2 * kHalf + slot];
       out[j] = s;
     }
   }
@@ -178,8 +185,12 @@ __global__ void __launch_bounds__(THREADS) k_bwd_cta(const BwdArgs p) {
   const bool cols = p.ws != nullptr;
   const uint32_t row_bytes = static_cast<uint32_t>(H) * S;  // multiple of 16
   const uint32_t rb = (row_bytes + 127u) & ~127u;
-  float* part = reinterpret_cast<float*>(smem + 2 * rb);       // dgamma[H], dbeta[H]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * rb + 8 * ((H + 3) & ~3));
+  // partials, thread-major so a warp's accesses hit 32 distinct banks: column
+  // (tid + THREADS k) * VEC + i lives at slot (k * VEC + i) * THREADS + tid of
+  // the dgamma half [0, THREADS NV VEC) and of the dbeta half after it
+  constexpr int kHalf = THREADS * NV * VEC;
+  float* part = reinterpret_cast<float*>(smem + 2 * rb);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * rb + 8 * kHalf);
   float2* red = reinterpret_cast<float2*>(reinterpret_cast<char*>(bar) + 16);  // [2][NW]
   const uint32_t s0 = smem_addr(smem);
   const uint32_t bar_a = smem_addr(bar);
@@ -190,12 +201,11 @@ __global__ void __launch_bounds__(THREADS) k_bwd_cta(const BwdArgs p) {
   if (cols)
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (ok[k])
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          part[(tid + THREADS * k) * VEC + e] = 0.f;
-          part[H + (tid + THREADS * k) * VEC + e] = 0.f;
-        }
+      for (int e = 0; e < VEC; ++e) {
+        part[(k * VEC + e) * THREADS + tid] = 0.f;
+        part[kHalf + (k * VEC + e) * THREADS + tid] = 0.f;
+      }
   if (tid == 0) {
     mbar_init(bar_a, 1);
     fence_mbar_init();
@@ -241,8 +251,9 @@ __global__ void __launch_bounds__(THREADS) k_bwd_cta(const BwdArgs p) {
         if (cols && !timed_out)
 #pragma unroll
           for (int i = 0; i < VEC; ++i) {
-            part[c * VEC + i] = fmaf(d[i], xh[k][i], part[c * VEC + i]);
-            part[H + c * VEC + i] += d[i];
+            float* sl = part + (k * VEC + i) * THREADS + tid;
+            sl[0] = fmaf(d[i], xh[k][i], sl[0]);
+            sl[kHalf] += d[i];
           }
       }
     }
@@ -292,8 +303,8 @@ __global__ void __launch_bounds__(THREADS) k_bwd_cta(const BwdArgs p) {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
           const int j = (tid + THREADS * k) * VEC + i;
-          out[j] = part[j];
-          out[H + j] = part[H + j];
+          out[j] = part[(k * VEC + i) * THREADS + tid];
+          out[H + j] = part[kHalf + (k * VEC + i) * THREADS + tid];
         }
   }
 }
@@ -359,21 +370,36 @@ __global__ void __launch_bounds__(THREADS) k_bwd_scalar(const BwdArgs p) {
   }
 }
 
-// dgamma_j = sum_b ws[b][0][j], dbeta_j = sum_b ws[b][1][j], b in order.
-__global__ void __launch_bounds__(256) k_colsum(const float* ws, int64_t G, int H, float* dgamma,
-                                                float* dbeta) {
+// dgamma_j = sum_b ws[b][0][j], dbeta_j = sum_b ws[b][1][j].  A block covers
+// 32 columns with 8 slices of the partials each (slice s takes b = s, s + 8,
+// ...); the 8 slice sums are then added in slice order, so the result does
+// not depend on scheduling.
+constexpr int kColCols = 32, kColSlices = 8;
+
+__global__ void __launch_bounds__(kColCols * kColSlices) k_colsum(const float* ws, int64_t G, int H,
+                                                                  float* dgamma, float* dbeta) {
+  __shared__ float part[kColSlices][kColCols];
   pdl_trigger();
   pdl_wait();
-  const int j = blockIdx.x * 256 + threadIdx.x;
-  if (j >= 2 * H) return;
-  float s = 0.f;
+  const int lc = threadIdx.x % kColCols, sl = threadIdx.x / kColCols;
+  const int j = blockIdx.x * kColCols + lc;
   const int64_t ld = 2 * static_cast<int64_t>(H);
-#pragma unroll 8
-  for (int64_t b = 0; b < G; ++b) s += ws[b * ld + j];
-  if (j < H)
-    dgamma[j] = s;
-  else
-    dbeta[j - H] = s;
+  float s = 0.f;
+  if (j < 2 * H) {
+#pragma unroll 4
+    for (int64_t b = sl; b < G; b += kColSlices) s += ws[b * ld + j];
+  }
+  part[sl][lc] = s;
+  __syncthreads();
+  if (sl == 0 && j < 2 * H) {
+    float t = part[0][lc];
+#pragma unroll
+    for (int q = 1; q < kColSlices; ++q) t += part[q][lc];
+    if (j < H)
+      dgamma[j] = t;
+    else
+      dbeta[j - H] = t;
+  }
 }
 
 // ------------------------------------------------------------------ host
@@ -423,11 +449,11 @@ struct Plan {
 };
 
 // One wave of resident CTAs, but no more than needed to give every CTA about
-// eight rows (fewer, fuller partials) and never fewer than one per SM.
+// four rows (fewer partials to write and sum) and never fewer than two per SM.
 int64_t grid_of(int64_t rows, int64_t per_cta_rows, int per_sm, const DeviceInfo& dev) {
   int64_t wave = static_cast<int64_t>(per_sm) * dev.sms;
-  int64_t want = (rows + 8 * per_cta_rows - 1) / (8 * per_cta_rows);
-  if (want < dev.sms) want = dev.sms;
+  int64_t want = (rows + 4 * per_cta_rows - 1) / (4 * per_cta_rows);
+  if (want < 2 * static_cast<int64_t>(dev.sms)) want = 2 * static_cast<int64_t>(dev.sms);
   int64_t g = want < wave ? want : wave;
   const int64_t need = (rows + per_cta_rows - 1) / per_cta_rows;
   if (g > need) g = need;
@@ -438,7 +464,7 @@ template <int DT, int NV, bool FULL>
 int plan_warp(const BwdArgs& p, const DeviceInfo& dev, Plan* pl) {
   pl->f = reinterpret_cast<const void*>(&k_bwd_warp<DT, NV, FULL>);
   pl->threads = kWarps * 32;
-  pl->smem = kWarps * 2u * static_cast<uint32_t>(p.H) * 4u;
+  pl->smem = kWarps * 2u * 32u * NV * Io<DT>::kVec * 4u;
   const int per_sm = resident(pl->f, pl->threads, static_cast<int>(pl->smem), dev);
   if (per_sm < 0) return ADDLN_ERR_CUDA;
   if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
@@ -453,8 +479,7 @@ int plan_cta(const BwdArgs& p, const DeviceInfo& dev, Plan* pl) {
   const uint32_t rb = (row_bytes + 127u) & ~127u;
   pl->f = reinterpret_cast<const void*>(&k_bwd_cta<DT, THREADS, NV, FULL>);
   pl->threads = THREADS;
-  pl->smem = 2u * rb + 8u * ((static_cast<uint32_t>(p.H) + 3u) & ~3u) + 16u +
-             2u * (THREADS / 32) * sizeof(float2);
+  pl->smem = 2u * rb + 8u * THREADS * NV * Io<DT>::kVec + 16u + 2u * (THREADS / 32) * sizeof(float2);
   if (pl->smem > static_cast<uint32_t>(dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
   const int per_sm = resident(pl->f, THREADS, static_cast<int>(pl->smem), dev);
   if (per_sm < 0) return ADDLN_ERR_CUDA;
@@ -560,7 +585,8 @@ int launch_bwd(int dtype, const void* dy, const void* a, const float* mean, cons
   }
   if (want_cols) {
     const int64_t cols = 2 * H;
-    e = launch_kernel(bw::k_colsum, dim3(static_cast<unsigned>((cols + 255) / 256)), dim3(256), 0,
+    e = launch_kernel(bw::k_colsum, dim3(static_cast<unsigned>((cols + bw::kColCols - 1) / bw::kColCols)),
+                      dim3(bw::kColCols * bw::kColSlices), 0,
                       c.stream, c.pdl, static_cast<const float*>(ws), partials,
                       static_cast<int>(H), dgamma, dbeta);
     if (e != cudaSuccess) {
