@@ -21,7 +21,21 @@
 
 namespace addln {
 
+// ------------------------------------------------------------ fp32 pairs
+// sm_100 and later execute an fp32 add, multiply or fma on a pair of values
+// as one instruction.  The vector paths of the row kernels keep their fp32
+// values as float2 pairs and do their element-wise arithmetic through these;
+// each is the correctly rounded scalar operation applied to .x and to .y.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 dup2(float s) { return make_float2(s, s); }
+
 // ------------------------------------------------------------ dtype traits
+// unpack / pack: a 16-byte vector to and from fp32 values; to_pairs /
+// from_pairs: the same as kVec/2 float2 pairs; sum_pairs: a = x + r for
+// each element of two vectors, as pairs (the exact fp32 value of each input,
+// one rounding of the sum).
 template <int DT>
 struct Io;
 
@@ -38,6 +52,21 @@ struct Io<kF32> {
   __device__ static __forceinline__ uint4 pack(const float* f) {
     return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                       __float_as_uint(f[3]));
+  }
+  __device__ static __forceinline__ void to_pairs(const uint4& u, float2* f) {
+    f[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+    f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+  }
+  __device__ static __forceinline__ uint4 from_pairs(const float2* f) {
+    return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
+                      __float_as_uint(f[1].y));
+  }
+  __device__ static __forceinline__ void sum_pairs(const uint4& x, const uint4& r, float2* a) {
+    float2 t[2], u[2];
+    to_pairs(x, t);
+    to_pairs(r, u);
+    a[0] = add2(t[0], u[0]);
+    a[1] = add2(t[1], u[1]);
   }
   __device__ static __forceinline__ float load1(const void* p, int64_t i) {
     return __ldg(static_cast<const float*>(p) + i);
@@ -69,6 +98,34 @@ struct Io<kF16> {
   __device__ static __forceinline__ uint4 pack(const float* f) {
     return make_uint4(f2w(f[0], f[1]), f2w(f[2], f[3]), f2w(f[4], f[5]), f2w(f[6], f[7]));
   }
+  __device__ static __forceinline__ void to_pairs(const uint4& u, float2* f) {
+    f[0] = w2f(u.x);
+    f[1] = w2f(u.y);
+    f[2] = w2f(u.z);
+    f[3] = w2f(u.w);
+  }
+  __device__ static __forceinline__ uint4 from_pairs(const float2* f) {
+    return make_uint4(f2w(f[0].x, f[0].y), f2w(f[1].x, f[1].y), f2w(f[2].x, f[2].y),
+                      f2w(f[3].x, f[3].y));
+  }
+  // Both halves of a word of X widened, then each added to the matching half
+  // of R by the mixed-precision add (f16 operand + f32 operand -> f32).
+  __device__ static __forceinline__ float2 word_sum(uint32_t xw, uint32_t rw) {
+    float2 o;
+    asm("{\n\t.reg .b16 x0, x1, r0, r1;\n\t.reg .f32 f0, f1;\n\t"
+        "mov.b32 {x0, x1}, %2;\n\tmov.b32 {r0, r1}, %3;\n\t"
+        "cvt.f32.f16 f0, x0;\n\tcvt.f32.f16 f1, x1;\n\t"
+        "add.rn.f32.f16 %0, r0, f0;\n\tadd.rn.f32.f16 %1, r1, f1;\n\t}"
+        : "=f"(o.x), "=f"(o.y)
+        : "r"(xw), "r"(rw));
+    return o;
+  }
+  __device__ static __forceinline__ void sum_pairs(const uint4& x, const uint4& r, float2* a) {
+    a[0] = word_sum(x.x, r.x);
+    a[1] = word_sum(x.y, r.y);
+    a[2] = word_sum(x.z, r.z);
+    a[3] = word_sum(x.w, r.w);
+  }
   __device__ static __forceinline__ float load1(const void* p, int64_t i) {
     unsigned short b = __ldg(static_cast<const unsigned short*>(p) + i);
     return __half2float(__ushort_as_half(b));
@@ -99,6 +156,32 @@ struct Io<kBF16> {
   }
   __device__ static __forceinline__ uint4 pack(const float* f) {
     return make_uint4(f2w(f[0], f[1]), f2w(f[2], f[3]), f2w(f[4], f[5]), f2w(f[6], f[7]));
+  }
+  __device__ static __forceinline__ void to_pairs(const uint4& u, float2* f) {
+    f[0] = w2f(u.x);
+    f[1] = w2f(u.y);
+    f[2] = w2f(u.z);
+    f[3] = w2f(u.w);
+  }
+  __device__ static __forceinline__ uint4 from_pairs(const float2* f) {
+    return make_uint4(f2w(f[0].x, f[0].y), f2w(f[1].x, f[1].y), f2w(f[2].x, f[2].y),
+                      f2w(f[3].x, f[3].y));
+  }
+  __device__ static __forceinline__ float2 word_sum(uint32_t xw, uint32_t rw) {
+    float2 o;
+    asm("{\n\t.reg .b16 x0, x1, r0, r1;\n\t.reg .f32 f0, f1;\n\t"
+        "mov.b32 {x0, x1}, %2;\n\tmov.b32 {r0, r1}, %3;\n\t"
+        "cvt.f32.bf16 f0, x0;\n\tcvt.f32.bf16 f1, x1;\n\t"
+        "add.rn.f32.bf16 %0, r0, f0;\n\tadd.rn.f32.bf16 %1, r1, f1;\n\t}"
+        : "=f"(o.x), "=f"(o.y)
+        : "r"(xw), "r"(rw));
+    return o;
+  }
+  __device__ static __forceinline__ void sum_pairs(const uint4& x, const uint4& r, float2* a) {
+    a[0] = word_sum(x.x, r.x);
+    a[1] = word_sum(x.y, r.y);
+    a[2] = word_sum(x.z, r.z);
+    a[3] = word_sum(x.w, r.w);
   }
   __device__ static __forceinline__ float load1(const void* p, int64_t i) {
     unsigned short b = __ldg(static_cast<const unsigned short*>(p) + i);
@@ -170,6 +253,12 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 
@@ -341,6 +430,55 @@ __device__ __forceinline__ Part thread_part(const float (&v)[NV][VEC], const boo
   for (int l = 1; l < L; ++l) M2 += sq[l];
   p.M2 = M2;
   return p;
+}
+
+// thread_part on values held as fp32 pairs.  SHIFT: subtract negK's
+// negation on the fly (the values are the unshifted sums); otherwise the
+// values are already shifted.  Pairs alternate between two accumulators, four
+// independent sums in all.
+template <int NV, int P, bool FULL, bool SHIFT>
+__device__ __forceinline__ Part thread_part2(const float2 (&v)[NV][P], const bool (&ok)[NV],
+                                             float2 negK) {
+  float2 acc[2] = {dup2(0.f), dup2(0.f)};
+  int cnt = 0;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    if (FULL || ok[k]) {
+#pragma unroll
+      for (int q = 0; q < P; ++q)
+        acc[q & 1] = add2(acc[q & 1], SHIFT ? add2(v[k][q], negK) : v[k][q]);
+      cnt += 2 * P;
+    }
+  }
+  const float sum = (acc[0].x + acc[1].x) + (acc[0].y + acc[1].y);
+  Part p;
+  p.n = static_cast<float>(cnt);
+  constexpr int kN = NV * P * 2;
+  if constexpr (FULL && (kN & (kN - 1)) == 0)
+    p.m = sum * (1.0f / kN);  // exact: a power of two
+  else
+    p.m = cnt ? __fdiv_rn(sum, p.n) : 0.f;
+  const float2 negm = dup2(-p.m);
+  float2 sq[2] = {dup2(0.f), dup2(0.f)};
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    if (FULL || ok[k]) {
+#pragma unroll
+      for (int q = 0; q < P; ++q) {
+        const float2 d = add2(SHIFT ? add2(v[k][q], negK) : v[k][q], negm);
+        sq[q & 1] = fma2(d, d, sq[q & 1]);
+      }
+    }
+  }
+  p.M2 = (sq[0].x + sq[1].x) + (sq[0].y + sq[1].y);
+  return p;
+}
+
+// normalise() on a pair of shifted values: ((v - m) * rstd) * g + b, the
+// same three roundings per element; negm = (-m, -m), rstd2 = (rstd, rstd).
+__device__ __forceinline__ float2 normalise2(float2 v, float2 negm, float2 rstd2, float2 g,
+                                             float2 b) {
+  return fma2(mul2(add2(v, negm), rstd2), g, b);
 }
 
 // y = gamma * (a - mean) * rstd + beta with mean = K + m; the deviation is

@@ -5,12 +5,15 @@
 //
 // TMA variant: thread 0 stages whole rows of X and R into shared memory with
 // one-dimensional bulk copies (cp.async.bulk, completion counted on an
-// mbarrier).  With two stages the copy of the CTA's next row is issued the
-// moment the current row lands, so it streams in while the current row is
-// reduced and normalised and every SM keeps row-sized requests outstanding.  Each thread moves its slice
-// from shared memory into registers once; the reduction and the normalisation
-// both run on those registers, and Y / A go straight to global memory with
-// 16-byte streaming stores.
+// mbarrier) into a ring of `stages` slots: the first `stages` rows are
+// requested at once, and a slot is refilled with the CTA's row `stages`
+// ahead as soon as every thread has moved the slot's row into registers.
+// The reduction and the normalisation both run on those registers, and Y / A
+// go straight to global memory with 16-byte streaming stores.  When a thread
+// holds at most 32 values, it also keeps gamma and beta of its columns in
+// registers for the CTA's lifetime: reloading them for every row (8 bytes a
+// column, twice the row's own 16-bit X and R) would make the L1 data path,
+// not HBM, the limit.
 //
 // Vector variant: the same kernel with 16-byte loads from global memory in
 // place of the staging copies (kept for comparison and for forced runs).
@@ -32,6 +35,7 @@ namespace addln {
 __device__ int g_device_error = 0;
 
 constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s
+constexpr int kMaxStages = 4;  // staging slots a CTA (one mbarrier each)
 
 // CTA-level all-reduce of per-warp partials: lane 0 of each warp has put its
 // warp's totals in red[0..NW); every warp reads red[lane % NW] and runs the
@@ -42,13 +46,57 @@ __device__ __forceinline__ Part cta_totals(const Part* red, int lane) {
   return butterfly<FULL, NW>(q);
 }
 
+// After a wait ran out: flags the device error and waits (bounded) for the
+// copies still in flight -- rows it .. it+stages-1 of the ring -- so that no
+// copy lands in shared memory the next CTA on this SM may reuse.
+__device__ __noinline__ void drain_after_timeout(uint64_t* bars, int stages, int64_t it,
+                                                 int64_t row, int64_t stride, int64_t rows) {
+  atomicExch(&g_device_error, ADDLN_ERR_DEVICE_TIMEOUT);
+  for (int j = 0; j < stages; ++j) {
+    const int64_t itj = it + j;
+    if (row + j * stride < rows)
+      mbar_wait_bounded(smem_addr(&bars[itj % stages]), static_cast<uint32_t>((itj / stages) & 1),
+                        kDrainLimitNs);
+  }
+}
+
+// a_0 = x_0 + r_0 from the first words of the staged rows (xs: X's stage;
+// rs: R's, 0 without R), rounded once like every other sum.
+template <int DT>
+__device__ __forceinline__ float first_sum(uint32_t xs, uint32_t rs) {
+  if constexpr (DT == kF32) {
+    const float x0 = __uint_as_float(ld_shared_u32(xs));
+    return rs ? x0 + __uint_as_float(ld_shared_u32(rs)) : x0;
+  } else {
+    const uint32_t xw = ld_shared_u32(xs);
+    return rs ? Io<DT>::word_sum(xw, ld_shared_u32(rs)).x : Io<DT>::w2f(xw).x;
+  }
+}
+
+// gamma / beta stay in registers (TMA path, at most 32 values a thread).
+template <int DT, int NV, bool TMA>
+__host__ __device__ constexpr bool cta_row_resident() {
+  return TMA && NV * Io<DT>::kVec <= 32;
+}
+
+// Register cap a thread: 128 with resident gamma / beta (four 128-thread CTAs
+// to an SM); otherwise by the fp32 values held (64 for 16); the vector path
+// also holds the loaded vectors.
+template <int DT, int THREADS, int NV, bool TMA>
+constexpr int cta_row_max_regs() {
+  return cta_row_resident<DT, NV, TMA>() ? 128 : !TMA ? 128 : NV * Io<DT>::kVec <= 16 ? 64 : 128;
+}
+
 // FULL: the row's 16-byte vectors divide evenly over the CTA's threads.
 template <int DT, int THREADS, int NV, bool TMA, bool FULL>
-__global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int stages) {
+__global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THREADS, NV, TMA>()))
+    k_cta_row(const RowArgs p, const int stages) {
   using IO = Io<DT>;
   constexpr int VEC = IO::kVec;
+  constexpr int P = VEC / 2;  // fp32 pairs per vector
   constexpr int S = IO::kBytes;
   constexpr int NW = THREADS / 32;
+  constexpr bool RES = cta_row_resident<DT, NV, TMA>();
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -59,8 +107,8 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
   const uint32_t rb = (row_bytes + 127u) & ~127u;
   const uint32_t slot = has_r ? 2u * rb : rb;
   const uint32_t data_bytes = TMA ? static_cast<uint32_t>(stages) * slot : 0u;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + data_bytes);
-  Part* red = reinterpret_cast<Part*>(smem + data_bytes + 16);  // [2][NW]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + data_bytes);  // [stages]
+  Part* red = reinterpret_cast<Part*>(smem + data_bytes + 8u * kMaxStages);  // [2][NW]
   const uint32_t smem0 = smem_addr(smem);
 
   bool ok[NV];
@@ -82,7 +130,7 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
   pdl_trigger();
   pdl_wait();  // the previous kernel's writes are visible from here on
 
-  // Thread 0: stage row `rr` of X (and R) into stage `s`.
+  // Thread 0: stage row `rr` of X (and R) into slot `s`.
   auto issue = [&](int s, int64_t rr) {
     const uint32_t bar = smem_addr(&bars[s]);
     mbar_arrive_expect_tx(bar, has_r ? 2u * row_bytes : row_bytes);
@@ -91,73 +139,71 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
     if (has_r)
       bulk_g2s(smem0 + s * slot + rb, static_cast<const char*>(p.r) + off, row_bytes, bar, policy);
   };
-
-  // Copies run stages-1 rows ahead.  With two or more stages the next copy is
-  // issued as soon as the current row has landed (into the stage the
-  // previous row just vacated), so each CTA's transfer of row i+1 overlaps
-  // its reduction of row i without front-loading the whole grid's rows into
-  // the first microseconds; with one stage it is issued once the row is in
-  // registers.
-  const int ahead = stages > 1 ? stages - 1 : 0;
   if constexpr (TMA) {
-    if (tid == 0) {
-      if (stages == 1) {
-        if (row < p.rows) issue(0, row);
-      } else {
-        for (int s = 0; s < ahead; ++s)
-          if (row + s * stride < p.rows) issue(s, row + s * stride);
+    if (tid == 0)
+      for (int s = 0; s < stages; ++s)
+        if (row + s * stride < p.rows) issue(s, row + s * stride);
+  }
+
+  // gamma / beta of this thread's columns, while the first rows stream in
+  float2 gr[RES ? NV : 1][RES ? P : 1], br[RES ? NV : 1][RES ? P : 1];
+  if constexpr (RES) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+#pragma unroll
+      for (int q = 0; q < P / 2; ++q) {
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), b = g;
+        if (ok[k]) {
+          const int c = tid + THREADS * k;
+          g = ld_param_f4(p.gamma + c * VEC + 4 * q);
+          b = ld_param_f4(p.beta + c * VEC + 4 * q);
+        }
+        gr[k][2 * q] = make_float2(g.x, g.y);
+        gr[k][2 * q + 1] = make_float2(g.z, g.w);
+        br[k][2 * q] = make_float2(b.x, b.y);
+        br[k][2 * q + 1] = make_float2(b.z, b.w);
       }
     }
   }
 
   for (int64_t it = 0; row < p.rows; ++it, row += stride) {
     const int64_t base = row * static_cast<int64_t>(H);
-    float v[NV][VEC];
+    // the row's sums a = x + r as fp32 pairs, each thread's slice in registers
+    float2 v[NV][P];
 #pragma unroll
     for (int k = 0; k < NV; ++k)
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
+      for (int q = 0; q < P; ++q) v[k][q] = dup2(0.f);
 
-    bool timed_out = false;
-    bool issued_ahead = false;
     float K;  // the row's shift: its first sum a_0
+    const int s = TMA ? static_cast<int>(it % stages) : 0;
     if constexpr (TMA) {
-      const int s = static_cast<int>(it % stages);
-      const uint32_t parity = static_cast<uint32_t>((it / stages) & 1);
-      timed_out = !mbar_wait_bounded(smem_addr(&bars[s]), parity, p.wait_limit_ns);
-      if (ahead > 0 && tid == 0 && !timed_out) {
-        // stage (it + ahead) % stages last held row it-1, which every thread
-        // finished reading before the previous iteration's barrier
-        const int64_t next = row + ahead * stride;
-        if (next < p.rows) {
-          issue(static_cast<int>((it + ahead) % stages), next);
-          issued_ahead = true;
-        }
+      // Thread 0 alone waits for the slot's copies; the barrier then releases
+      // the other threads (ordered after its observation of the completed
+      // phase) and tells every thread whether the wait ran out.
+      bool landed = true;
+      if (tid == 0)
+        landed = mbar_wait_bounded(smem_addr(&bars[s]), static_cast<uint32_t>((it / stages) & 1),
+                                   p.wait_limit_ns);
+      if (__syncthreads_or(!landed)) {
+        if (tid == 0) drain_after_timeout(bars, stages, it, row, stride, p.rows);
+        return;
       }
       const uint32_t xs = smem0 + s * slot;
-#pragma unroll
-      for (int k = 0; k < NV; ++k)
-        if (ok[k]) IO::unpack(ld_shared_v4(xs + (tid + THREADS * k) * 16), v[k]);
       if (has_r) {
 #pragma unroll
-        for (int k = 0; k < NV; ++k) {
-          if (ok[k]) {
-            float t[VEC];
-            IO::unpack(ld_shared_v4(xs + rb + (tid + THREADS * k) * 16), t);
+        for (int k = 0; k < NV; ++k)
+          if (ok[k])
+            IO::sum_pairs(ld_shared_v4(xs + (tid + THREADS * k) * 16),
+                          ld_shared_v4(xs + rb + (tid + THREADS * k) * 16), v[k]);
+      } else {
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) v[k][e] += t[e];
-          }
-        }
+        for (int k = 0; k < NV; ++k)
+          if (ok[k]) IO::to_pairs(ld_shared_v4(xs + (tid + THREADS * k) * 16), v[k]);
       }
       // a_0 from the staged copy (a broadcast read; unaffected by any global
       // store, so A may alias R)
-      float t[VEC];
-      IO::unpack(ld_shared_v4(xs), t);
-      K = t[0];
-      if (has_r) {
-        IO::unpack(ld_shared_v4(xs + rb), t);
-        K += t[0];
-      }
+      K = first_sum<DT>(xs, has_r ? xs + rb : 0u);
     } else {
       // a_0 from global memory, read before the barrier below; every global
       // store of this row comes after that barrier, so in-place is safe
@@ -172,73 +218,66 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
 #pragma unroll
         for (int k = 0; k < NV; ++k)
           if (ok[k]) rv[k] = ld_stream_v4(rrow + static_cast<int64_t>(tid + THREADS * k) * 16);
-      }
 #pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        if (ok[k]) {
-          IO::unpack(xv[k], v[k]);
-          if (has_r) {
-            float t[VEC];
-            IO::unpack(rv[k], t);
+        for (int k = 0; k < NV; ++k)
+          if (ok[k]) IO::sum_pairs(xv[k], rv[k], v[k]);
+      } else {
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) v[k][e] += t[e];
-          }
-        }
+        for (int k = 0; k < NV; ++k)
+          if (ok[k]) IO::to_pairs(xv[k], v[k]);
       }
     }
+    const float2 negK = dup2(-K);
 
-    // ---- TMA path: A = X + R rounded to the dtype, stored at once
-    if (TMA && p.a != nullptr && !timed_out) {
-      char* arow = static_cast<char*>(p.a) + base * S;
+    // ---- TMA path: A = X + R rounded to the dtype, stored at once; then the
+    // values are shifted in place
+    if constexpr (TMA) {
+      if (p.a != nullptr) {
+        char* arow = static_cast<char*>(p.a) + base * S;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          if (ok[k])
+            st_stream_v4(arow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::from_pairs(v[k]));
+      }
 #pragma unroll
       for (int k = 0; k < NV; ++k)
-        if (ok[k]) st_stream_v4(arow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::pack(v[k]));
+#pragma unroll
+        for (int q = 0; q < P; ++q) v[k][q] = add2(v[k][q], negK);
     }
 
     // ---- statistics: per-thread two-pass on the shifted row, warp
     // butterfly, then the CTA merge of the warp partials
-    Part st;
-    if constexpr (TMA) {
-#pragma unroll
-      for (int k = 0; k < NV; ++k)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) v[k][e] -= K;
-      st = thread_part<NV, VEC, FULL>(v, ok, 0.f);
-    } else {
-      st = thread_part<NV, VEC, FULL>(v, ok, K);
-    }
+    Part st = thread_part2<NV, P, FULL, !TMA>(v, ok, negK);
     st = butterfly<FULL, 32>(st);
     Part* rbuf = red + (it & 1) * NW;
     if (lane == 0) rbuf[warp] = st;
 
     if constexpr (TMA) {
-      // Also the point after which no thread reads stage s any more.
-      if (__syncthreads_or(timed_out)) {
-        if (tid == 0) {
-          // copies in flight: rows it .. it+ahead-1, plus it+ahead if issued
-          atomicExch(&g_device_error, ADDLN_ERR_DEVICE_TIMEOUT);
-          const int pending = ahead > 0 ? ahead + (issued_ahead ? 1 : 0) : 1;
-          for (int j = 0; j < pending; ++j) {
-            const int64_t itj = it + j;
-            if (row + j * stride < p.rows)
-              mbar_wait_bounded(smem_addr(&bars[itj % stages]),
-                                static_cast<uint32_t>((itj / stages) & 1), kDrainLimitNs);
-          }
-        }
-        return;
-      }
-      if (ahead == 0 && tid == 0) {
-        const int64_t next = row + stride;
-        if (next < p.rows) issue(0, next);
+      // Also the point after which no thread reads slot s any more.
+      __syncthreads();
+      if (tid == 0) {
+        const int64_t next = row + stages * stride;
+        if (next < p.rows) issue(s, next);
       }
     } else {
       __syncthreads();
+      // the vector path shifts after its A store, which must follow the barrier
+      if (p.a != nullptr) {
+        char* arow = static_cast<char*>(p.a) + base * S;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          if (ok[k])
+            st_stream_v4(arow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::from_pairs(v[k]));
+      }
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int q = 0; q < P; ++q) v[k][q] = add2(v[k][q], negK);
     }
 
     const Part tot = cta_totals<FULL, NW>(rbuf, lane);
-    const float m = tot.m;
     const float rstd = row_rstd(tot.M2, p.inv_h, p.eps);
-    const float Kn = TMA ? 0.f : K;  // shift still to remove before normalising
+    const float2 negm = dup2(-tot.m), rstd2 = dup2(rstd);
 
     // ---- normalise + affine from registers, store
     char* yrow = static_cast<char*>(p.y) + base * S;
@@ -246,27 +285,25 @@ __global__ void __launch_bounds__(THREADS) k_cta_row(const RowArgs p, const int 
     for (int k = 0; k < NV; ++k) {
       if (ok[k]) {
         const int c = tid + THREADS * k;
-        float o[VEC];
+        float2 o[P];
+        if constexpr (RES) {
 #pragma unroll
-        for (int q = 0; q < VEC / 4; ++q) {
-          const float4 g = ld_param_f4(p.gamma + c * VEC + 4 * q);
-          const float4 b = ld_param_f4(p.beta + c * VEC + 4 * q);
-          o[4 * q + 0] = normalise(v[k][4 * q + 0], Kn, m, rstd, g.x, b.x);
-          o[4 * q + 1] = normalise(v[k][4 * q + 1], Kn, m, rstd, g.y, b.y);
-          o[4 * q + 2] = normalise(v[k][4 * q + 2], Kn, m, rstd, g.z, b.z);
-          o[4 * q + 3] = normalise(v[k][4 * q + 3], Kn, m, rstd, g.w, b.w);
+          for (int q = 0; q < P; ++q) o[q] = normalise2(v[k][q], negm, rstd2, gr[k][q], br[k][q]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < P / 2; ++q) {
+            const float4 g = ld_param_f4(p.gamma + c * VEC + 4 * q);
+            const float4 b = ld_param_f4(p.beta + c * VEC + 4 * q);
+            o[2 * q] = normalise2(v[k][2 * q], negm, rstd2, make_float2(g.x, g.y), make_float2(b.x, b.y));
+            o[2 * q + 1] =
+                normalise2(v[k][2 * q + 1], negm, rstd2, make_float2(g.z, g.w), make_float2(b.z, b.w));
+          }
         }
-        st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::pack(o));
+        st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::from_pairs(o));
       }
     }
-    if (!TMA && p.a != nullptr) {
-      char* arow = static_cast<char*>(p.a) + base * S;
-#pragma unroll
-      for (int k = 0; k < NV; ++k)
-        if (ok[k]) st_stream_v4(arow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::pack(v[k]));
-    }
     if (tid == 0) {
-      if (p.mean != nullptr) p.mean[row] = K + m;
+      if (p.mean != nullptr) p.mean[row] = K + tot.m;
       if (p.rstd != nullptr) p.rstd[row] = rstd;
     }
   }
@@ -389,19 +426,50 @@ int launch_row_t(const RowArgs& p, const LaunchCtx& c) {
   const uint32_t row_bytes = static_cast<uint32_t>(p.H) * S;
   const uint32_t rb = (row_bytes + 127u) & ~127u;
   const uint32_t slot = p.r ? 2u * rb : rb;
-  const uint32_t extra = 16u + 2u * (THREADS / 32) * sizeof(Part);
-  int stages = 0;
+  const uint32_t extra = 8u * kMaxStages + 2u * (THREADS / 32) * sizeof(Part);
+  const void* f = reinterpret_cast<const void*>(&k_cta_row<DT, THREADS, NV, TMA, FULL>);
+  int stages = 0, per_sm = 0;
   uint32_t smem = extra;
   if (TMA) {
-    // One staged row per CTA by default: the shared memory a second stage
-    // takes costs more resident CTAs (rows reduced in parallel) than its
-    // prefetch gains (measured on 2048x4096 fp16 and 32768x8192 bf16).
-    stages = c.stages > 0 ? c.stages : 1;
-    smem = stages * slot + extra;
-    if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
+    if (c.stages > 0) {
+      if (c.stages > kMaxStages) return ADDLN_ERR_UNSUPPORTED;
+      stages = c.stages;
+      smem = stages * slot + extra;
+      if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
+      per_sm = resident_ctas(f, THREADS, static_cast<int>(smem), c.dev);
+    } else if (cta_row_resident<DT, NV, TMA>()) {
+      // Registers bound the CTAs an SM holds.  Two slots a CTA, unless the
+      // second would cost resident CTAs, or the kernel also writes A (writes
+      // then weigh as much as reads) and every CTA has more than eight rows
+      // to do: there one slot measured faster (32768 x 8192 bf16), two
+      // everywhere else (2048 .. 17024 x 4096 fp16, 2048 x 8192 bf16).
+      smem = slot + extra;
+      if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
+      stages = 1;
+      per_sm = resident_ctas(f, THREADS, static_cast<int>(smem), c.dev);
+      if (per_sm < 0) return ADDLN_ERR_CUDA;
+      const bool long_with_a =
+          p.a != nullptr && p.rows > 8 * static_cast<int64_t>(per_sm) * c.dev.sms;
+      const uint32_t smem2 = 2 * slot + extra;
+      if (!long_with_a && smem2 <= static_cast<uint32_t>(c.dev.smem_optin)) {
+        const int n2 = resident_ctas(f, THREADS, static_cast<int>(smem2), c.dev);
+        if (n2 < 0) return ADDLN_ERR_CUDA;
+        if (n2 >= per_sm) {
+          stages = 2;
+          smem = smem2;
+        }
+      }
+    } else {
+      // One slot: a second one costs more resident CTAs (rows reduced in
+      // parallel) than its prefetch gains.
+      stages = 1;
+      smem = slot + extra;
+      if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
+      per_sm = resident_ctas(f, THREADS, static_cast<int>(smem), c.dev);
+    }
+  } else {
+    per_sm = resident_ctas(f, THREADS, static_cast<int>(smem), c.dev);
   }
-  const void* f = reinterpret_cast<const void*>(&k_cta_row<DT, THREADS, NV, TMA, FULL>);
-  const int per_sm = resident_ctas(f, THREADS, static_cast<int>(smem), c.dev);
   if (per_sm < 0) return ADDLN_ERR_CUDA;
   if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
   const int64_t grid = persistent_grid(p.rows, per_sm, c);

@@ -1,8 +1,8 @@
 // One warp per row: fused residual add + LayerNorm for short rows (H <= 1024).
 //
 // Each lane loads its share of the row of X and R with 16-byte streaming
-// loads (vector path) or element loads (scalar path, any alignment) and adds
-// them in fp32 registers.  A (when requested) is stored straight away.  The
+// loads (vector path, values then held as fp32 pairs) or element loads
+// (scalar path, any alignment) and adds them in fp32 registers.  A (when requested) is stored straight away.  The
 // values are then shifted by the row's first sum a_0, which lane 0 holds and
 // broadcasts by shuffle; each lane takes two-pass statistics of its own
 // values and the warp merges them with a xor butterfly of Chan updates.  The
@@ -17,11 +17,22 @@ namespace addln {
 constexpr int kWarpCtaThreads = 256;  // 8 rows per CTA
 constexpr int kRowsPerCta = kWarpCtaThreads / 32;
 
-// FULL: the row's vectors (elements) divide evenly over the 32 lanes.
-template <int DT, int NV, bool VECTOR, bool FULL>
-__global__ void __launch_bounds__(kWarpCtaThreads, 2) k_warp_row(const RowArgs p) {
+// Register cap a lane: 64 while it holds at most 24 values (four 256-thread
+// CTAs to an SM); above that 80 for 16-bit rows (three), 96 for fp32 ones,
+// whose eight vectors need more addresses (two).  None of them spills.
+template <int DT, int NV>
+constexpr int warp_row_max_regs() {
+  return NV * Io<DT>::kVec <= 24 ? 64 : DT == kF32 ? 96 : 80;
+}
+
+// Vector path: 16-byte loads, values held as fp32 pairs.  FULL: the row's
+// vectors divide evenly over the 32 lanes.
+template <int DT, int NV, bool FULL>
+__global__ void __launch_bounds__(kWarpCtaThreads) __maxnreg__((warp_row_max_regs<DT, NV>()))
+    k_warp_row_vec(const RowArgs p) {
   using IO = Io<DT>;
-  constexpr int VEC = VECTOR ? IO::kVec : 1;
+  constexpr int VEC = IO::kVec;
+  constexpr int P = VEC / 2;
   constexpr int S = IO::kBytes;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
@@ -36,105 +47,135 @@ __global__ void __launch_bounds__(kWarpCtaThreads, 2) k_warp_row(const RowArgs p
 #pragma unroll
   for (int k = 0; k < NV; ++k) ok[k] = FULL || (lane + 32 * k) < nvec;
 
-  float v[NV][VEC];
+  float2 v[NV][P];
 #pragma unroll
   for (int k = 0; k < NV; ++k)
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
+    for (int q = 0; q < P; ++q) v[k][q] = dup2(0.f);
 
   // ---- load X and R once, add in fp32
-  if constexpr (VECTOR) {
-    const char* xrow = static_cast<const char*>(p.x) + base * S;
-    uint4 xv[NV], rv[NV];
+  const char* xrow = static_cast<const char*>(p.x) + base * S;
+  uint4 xv[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (ok[k]) xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(lane + 32 * k) * 16);
+  if (p.r != nullptr) {
+    const char* rrow = static_cast<const char*>(p.r) + base * S;
+    uint4 rv[NV];
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (ok[k]) xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(lane + 32 * k) * 16);
-    if (p.r != nullptr) {
-      const char* rrow = static_cast<const char*>(p.r) + base * S;
+      if (ok[k]) rv[k] = ld_stream_v4(rrow + static_cast<int64_t>(lane + 32 * k) * 16);
 #pragma unroll
-      for (int k = 0; k < NV; ++k)
-        if (ok[k]) rv[k] = ld_stream_v4(rrow + static_cast<int64_t>(lane + 32 * k) * 16);
-    }
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      if (ok[k]) {
-        IO::unpack(xv[k], v[k]);
-        if (p.r != nullptr) {
-          float t[VEC];
-          IO::unpack(rv[k], t);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) v[k][e] += t[e];
-        }
-      }
-    }
+    for (int k = 0; k < NV; ++k)
+      if (ok[k]) IO::sum_pairs(xv[k], rv[k], v[k]);
   } else {
-    float t[NV];
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (ok[k]) v[k][0] = IO::load1(p.x, base + lane + 32 * k);
-    if (p.r != nullptr) {
-#pragma unroll
-      for (int k = 0; k < NV; ++k)
-        if (ok[k]) t[k] = IO::load1(p.r, base + lane + 32 * k);
-#pragma unroll
-      for (int k = 0; k < NV; ++k)
-        if (ok[k]) v[k][0] += t[k];
-    }
+      if (ok[k]) IO::to_pairs(xv[k], v[k]);
   }
 
   // ---- A = X + R rounded to the dtype; each lane writes only what it read
   if (p.a != nullptr) {
-    if constexpr (VECTOR) {
-      char* arow = static_cast<char*>(p.a) + base * S;
+    char* arow = static_cast<char*>(p.a) + base * S;
 #pragma unroll
-      for (int k = 0; k < NV; ++k)
-        if (ok[k]) st_stream_v4(arow + static_cast<int64_t>(lane + 32 * k) * 16, IO::pack(v[k]));
-    } else {
+    for (int k = 0; k < NV; ++k)
+      if (ok[k]) st_stream_v4(arow + static_cast<int64_t>(lane + 32 * k) * 16, IO::from_pairs(v[k]));
+  }
+
+  // ---- row statistics on the shifted row: per-lane two-pass, warp butterfly
+  const float K = __shfl_sync(0xffffffffu, v[0][0].x, 0);  // a_0, held by lane 0
+  const float2 negK = dup2(-K);
 #pragma unroll
-      for (int k = 0; k < NV; ++k)
-        if (ok[k]) IO::store1(p.a, base + lane + 32 * k, v[k][0]);
+  for (int k = 0; k < NV; ++k)
+#pragma unroll
+    for (int q = 0; q < P; ++q) v[k][q] = add2(v[k][q], negK);
+  Part st = thread_part2<NV, P, FULL, false>(v, ok, negK);
+  st = butterfly<FULL, 32>(st);
+  const float rstd = row_rstd(st.M2, p.inv_h, p.eps);
+  const float2 negm = dup2(-st.m), rstd2 = dup2(rstd);
+
+  // ---- normalise + affine, store
+  char* yrow = static_cast<char*>(p.y) + base * S;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    if (ok[k]) {
+      const int c = lane + 32 * k;
+      float2 o[P];
+#pragma unroll
+      for (int q = 0; q < P / 2; ++q) {
+        const float4 g = ld_param_f4(p.gamma + c * VEC + 4 * q);
+        const float4 b = ld_param_f4(p.beta + c * VEC + 4 * q);
+        o[2 * q] = normalise2(v[k][2 * q], negm, rstd2, make_float2(g.x, g.y), make_float2(b.x, b.y));
+        o[2 * q + 1] =
+            normalise2(v[k][2 * q + 1], negm, rstd2, make_float2(g.z, g.w), make_float2(b.z, b.w));
+      }
+      st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::from_pairs(o));
     }
+  }
+  if (lane == 0) {
+    if (p.mean != nullptr) p.mean[row] = K + st.m;
+    if (p.rstd != nullptr) p.rstd[row] = rstd;
+  }
+}
+
+// Element path (any alignment): one element per lane per slot.  FULL: the
+// row's elements divide evenly over the 32 lanes.
+template <int DT, int NV, bool FULL>
+__global__ void __launch_bounds__(kWarpCtaThreads, 2) k_warp_row(const RowArgs p) {
+  using IO = Io<DT>;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
+  pdl_trigger();
+  pdl_wait();
+  if (row >= p.rows) return;  // whole warp leaves together
+  const int H = p.H;
+  const int64_t base = row * static_cast<int64_t>(H);  // element offset of the row
+
+  bool ok[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) ok[k] = FULL || (lane + 32 * k) < H;
+
+  float v[NV][1];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) v[k][0] = 0.f;
+
+  // ---- load X and R once, add in fp32
+  float t[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (ok[k]) v[k][0] = IO::load1(p.x, base + lane + 32 * k);
+  if (p.r != nullptr) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (ok[k]) t[k] = IO::load1(p.r, base + lane + 32 * k);
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (ok[k]) v[k][0] += t[k];
+  }
+
+  // ---- A = X + R rounded to the dtype; each lane writes only what it read
+  if (p.a != nullptr) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (ok[k]) IO::store1(p.a, base + lane + 32 * k, v[k][0]);
   }
 
   // ---- row statistics on the shifted row: per-lane two-pass, warp butterfly
   const float K = __shfl_sync(0xffffffffu, v[0][0], 0);  // a_0, held by lane 0
 #pragma unroll
-  for (int k = 0; k < NV; ++k)
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) v[k][e] -= K;
-  Part st = thread_part<NV, VEC, FULL>(v, ok, 0.f);
+  for (int k = 0; k < NV; ++k) v[k][0] -= K;
+  Part st = thread_part<NV, 1, FULL>(v, ok, 0.f);
   st = butterfly<FULL, 32>(st);
   const float m = st.m;
   const float rstd = row_rstd(st.M2, p.inv_h, p.eps);
 
   // ---- normalise + affine, store
-  if constexpr (VECTOR) {
-    char* yrow = static_cast<char*>(p.y) + base * S;
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      if (ok[k]) {
-        const int c = lane + 32 * k;
-        float o[VEC];
-#pragma unroll
-        for (int q = 0; q < VEC / 4; ++q) {
-          const float4 g = ld_param_f4(p.gamma + c * VEC + 4 * q);
-          const float4 b = ld_param_f4(p.beta + c * VEC + 4 * q);
-          o[4 * q + 0] = normalise(v[k][4 * q + 0], 0.f, m, rstd, g.x, b.x);
-          o[4 * q + 1] = normalise(v[k][4 * q + 1], 0.f, m, rstd, g.y, b.y);
-          o[4 * q + 2] = normalise(v[k][4 * q + 2], 0.f, m, rstd, g.z, b.z);
-          o[4 * q + 3] = normalise(v[k][4 * q + 3], 0.f, m, rstd, g.w, b.w);
-        }
-        st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::pack(o));
-      }
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      if (ok[k]) {
-        const int j = lane + 32 * k;
-        const float g = __ldg(p.gamma + j), b = __ldg(p.beta + j);
-        IO::store1(p.y, base + j, normalise(v[k][0], 0.f, m, rstd, g, b));
-      }
+  for (int k = 0; k < NV; ++k) {
+    if (ok[k]) {
+      const int j = lane + 32 * k;
+      const float g = __ldg(p.gamma + j), b = __ldg(p.beta + j);
+      IO::store1(p.y, base + j, normalise(v[k][0], 0.f, m, rstd, g, b));
     }
   }
   if (lane == 0) {
@@ -150,9 +191,13 @@ static int launch(const RowArgs& p, const LaunchCtx& c) {
   constexpr int VEC = VECTOR ? Io<DT>::kVec : 1;
   const bool full = (p.H / VEC) == 32 * NV;
   const dim3 grid(static_cast<unsigned>(blocks));
-  const cudaError_t e =
-      full ? launch_kernel(k_warp_row<DT, NV, VECTOR, true>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p)
-           : launch_kernel(k_warp_row<DT, NV, VECTOR, false>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p);
+  cudaError_t e;
+  if constexpr (VECTOR)
+    e = full ? launch_kernel(k_warp_row_vec<DT, NV, true>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p)
+             : launch_kernel(k_warp_row_vec<DT, NV, false>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p);
+  else
+    e = full ? launch_kernel(k_warp_row<DT, NV, true>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p)
+             : launch_kernel(k_warp_row<DT, NV, false>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p);
   if (e != cudaSuccess) note_cuda_error(static_cast<int>(e));
   return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
