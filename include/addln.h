@@ -260,9 +260,9 @@ int addln_set_pdl(int on);
 
 /*
  * Test and benchmark only.  Shape of the TMA CTA-per-row kernel: `threads`
- * per CTA (64, 128, 256 or 512; 16-bit rows of at most 4096 elements; 0 =
- * chosen from H) and `stages` rows staged per CTA (1..8; 0 = chosen from the
- * shared memory size).  A shape that cannot run a call makes it return
+ * per CTA (128, 256 or 512; 16-bit rows of at most 4096 elements; 0 =
+ * chosen from H) and `stages` rows staged per CTA (1..4; 0 = chosen from the
+ * registers and shared memory the kernel takes).  A shape that cannot run a call makes it return
  * ADDLN_ERR_UNSUPPORTED.  Returns the previous thread setting, or
  * ADDLN_ERR_SHAPE for a value out of range.
  */

@@ -443,9 +443,8 @@ int64_t addln_set_grid_cap(int64_t ctas) { return g_grid_cap.exchange(ctas < 0 ?
 int addln_set_pdl(int on) { return g_pdl.exchange(on != 0 ? 1 : 0); }
 
 int addln_set_cta_shape(int threads, int stages) {
-  if (threads != 0 && threads != 64 && threads != 128 && threads != 256 && threads != 512)
-    return ADDLN_ERR_SHAPE;
-  if (stages < 0 || stages > 8) return ADDLN_ERR_SHAPE;
+  if (threads != 0 && threads != 128 && threads != 256 && threads != 512) return ADDLN_ERR_SHAPE;
+  if (stages < 0 || stages > 4) return ADDLN_ERR_SHAPE;
   const int prev = g_cta_threads.exchange(threads);
   g_stages.exchange(stages);
   return prev;

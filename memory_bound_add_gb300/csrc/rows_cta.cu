@@ -47,29 +47,18 @@ __device__ __forceinline__ Part cta_totals(const Part* red, int lane) {
 }
 
 // After a wait ran out: flags the device error and waits (bounded) for the
-// copies still in flight -- rows it .. it+stages-1 of the ring -- so that no
-// copy lands in shared memory the next CTA on this SM may reuse.
-__device__ __noinline__ void drain_after_timeout(uint64_t* bars, int stages, int64_t it,
+// copies still in flight -- every warp's chunk of rows it .. it+stages-1 of
+// the ring -- so that no copy lands in shared memory the next CTA on this SM
+// may reuse.
+__device__ __noinline__ void drain_after_timeout(uint64_t* bars, int stages, int nw, int64_t it,
                                                  int64_t row, int64_t stride, int64_t rows) {
   atomicExch(&g_device_error, ADDLN_ERR_DEVICE_TIMEOUT);
   for (int j = 0; j < stages; ++j) {
     const int64_t itj = it + j;
-    if (row + j * stride < rows)
-      mbar_wait_bounded(smem_addr(&bars[itj % stages]), static_cast<uint32_t>((itj / stages) & 1),
-                        kDrainLimitNs);
-  }
-}
-
-// a_0 = x_0 + r_0 from the first words of the staged rows (xs: X's stage;
-// rs: R's, 0 without R), rounded once like every other sum.
-template <int DT>
-__device__ __forceinline__ float first_sum(uint32_t xs, uint32_t rs) {
-  if constexpr (DT == kF32) {
-    const float x0 = __uint_as_float(ld_shared_u32(xs));
-    return rs ? x0 + __uint_as_float(ld_shared_u32(rs)) : x0;
-  } else {
-    const uint32_t xw = ld_shared_u32(xs);
-    return rs ? Io<DT>::word_sum(xw, ld_shared_u32(rs)).x : Io<DT>::w2f(xw).x;
+    if (row + j * stride >= rows) continue;
+    for (int w = 0; w < nw; ++w)
+      mbar_wait_bounded(smem_addr(&bars[(itj % stages) * nw + w]),
+                        static_cast<uint32_t>((itj / stages) & 1), kDrainLimitNs);
   }
 }
 
@@ -80,22 +69,43 @@ __host__ __device__ constexpr bool cta_row_resident() {
 }
 
 // Register cap a thread: 128 with resident gamma / beta (four 128-thread CTAs
-// to an SM); otherwise by the fp32 values held (64 for 16); the vector path
-// also holds the loaded vectors.
-template <int DT, int THREADS, int NV, bool TMA>
+// to an SM; 136, three, for the ragged-row variant, which otherwise spills);
+// otherwise by the fp32 values held (64 for 16); the vector path also holds
+// the loaded vectors.
+template <int DT, int THREADS, int NV, bool TMA, bool FULL>
 constexpr int cta_row_max_regs() {
-  return cta_row_resident<DT, NV, TMA>() ? 128 : !TMA ? 128 : NV * Io<DT>::kVec <= 16 ? 64 : 128;
+  return cta_row_resident<DT, NV, TMA>() ? (FULL || THREADS > 256 ? 128 : 136)
+         : !TMA                         ? 128
+         : NV * Io<DT>::kVec <= 16      ? 64
+                                        : 128;
 }
 
+// A warp's partial statistics of a row, with the shift they are taken around.
+struct WarpPart {
+  float K;  // the warp's shift: the first sum of its chunk
+  float n;
+  float m;  // mean of (a - K) over the warp's n values
+  float M2;
+};
+
 // FULL: the row's 16-byte vectors divide evenly over the CTA's threads.
+//
+// Warp w owns the contiguous chunk of vectors [w*32*NV, (w+1)*32*NV) of every
+// row (lane l, slot k: vector w*32*NV + 32*k + l), so on the TMA path each
+// warp's share of X and R arrives by its own pair of bulk copies, completing
+// its own mbarrier, and the warp starts on it as soon as it lands.  Each warp
+// shifts its values by the first sum of its chunk (Chan, Golub and LeVeque's
+// shifted data, per warp); the CTA merge first moves every warp's mean to
+// warp 0's shift, K_0 - the row's first sum a_0 - and then combines.
 template <int DT, int THREADS, int NV, bool TMA, bool FULL>
-__global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THREADS, NV, TMA>()))
+__global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THREADS, NV, TMA, FULL>()))
     k_cta_row(const RowArgs p, const int stages) {
   using IO = Io<DT>;
   constexpr int VEC = IO::kVec;
   constexpr int P = VEC / 2;  // fp32 pairs per vector
   constexpr int S = IO::kBytes;
   constexpr int NW = THREADS / 32;
+  constexpr int CV = 32 * NV;  // vectors in a warp's chunk
   constexpr bool RES = cta_row_resident<DT, NV, TMA>();
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -107,13 +117,19 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
   const uint32_t rb = (row_bytes + 127u) & ~127u;
   const uint32_t slot = has_r ? 2u * rb : rb;
   const uint32_t data_bytes = TMA ? static_cast<uint32_t>(stages) * slot : 0u;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + data_bytes);  // [stages]
-  Part* red = reinterpret_cast<Part*>(smem + data_bytes + 8u * kMaxStages);  // [2][NW]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + data_bytes);  // [stages][NW]
+  WarpPart* red = reinterpret_cast<WarpPart*>(smem + data_bytes + 8u * kMaxStages * NW);  // [2][NW]
   const uint32_t smem0 = smem_addr(smem);
 
+  const int v0 = warp * CV + lane;  // this thread's first vector
   bool ok[NV];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) ok[k] = FULL || (tid + THREADS * k) < nvec;
+  for (int k = 0; k < NV; ++k) ok[k] = FULL || v0 + 32 * k < nvec;
+
+  // bytes of X in this warp's chunk (0 for a warp past the end of a short row)
+  const int cvecs = FULL ? CV : min(CV, max(0, nvec - warp * CV));
+  const uint32_t chunk_bytes = static_cast<uint32_t>(cvecs) * 16u;
+  const uint32_t chunk_off = static_cast<uint32_t>(warp * CV) * 16u;
 
   const int64_t stride = gridDim.x;
   int64_t row = blockIdx.x;
@@ -121,7 +137,7 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
 
   if constexpr (TMA) {
     if (tid == 0) {
-      for (int s = 0; s < stages; ++s) mbar_init(smem_addr(&bars[s]), 1);
+      for (int s = 0; s < stages * NW; ++s) mbar_init(smem_addr(&bars[s]), 1);
       fence_mbar_init();
     }
     __syncthreads();
@@ -130,17 +146,19 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
   pdl_trigger();
   pdl_wait();  // the previous kernel's writes are visible from here on
 
-  // Thread 0: stage row `rr` of X (and R) into slot `s`.
+  // Lane 0 of each warp: stage the warp's chunk of row `rr` into slot `s`.
   auto issue = [&](int s, int64_t rr) {
-    const uint32_t bar = smem_addr(&bars[s]);
-    mbar_arrive_expect_tx(bar, has_r ? 2u * row_bytes : row_bytes);
-    const int64_t off = rr * static_cast<int64_t>(row_bytes);
-    bulk_g2s(smem0 + s * slot, static_cast<const char*>(p.x) + off, row_bytes, bar, policy);
-    if (has_r)
-      bulk_g2s(smem0 + s * slot + rb, static_cast<const char*>(p.r) + off, row_bytes, bar, policy);
+    const uint32_t bar = smem_addr(&bars[s * NW + warp]);
+    mbar_arrive_expect_tx(bar, has_r ? 2u * chunk_bytes : chunk_bytes);
+    if (chunk_bytes != 0) {
+      const int64_t off = rr * static_cast<int64_t>(row_bytes) + chunk_off;
+      const uint32_t dst = smem0 + s * slot + chunk_off;
+      bulk_g2s(dst, static_cast<const char*>(p.x) + off, chunk_bytes, bar, policy);
+      if (has_r) bulk_g2s(dst + rb, static_cast<const char*>(p.r) + off, chunk_bytes, bar, policy);
+    }
   };
   if constexpr (TMA) {
-    if (tid == 0)
+    if (lane == 0)
       for (int s = 0; s < stages; ++s)
         if (row + s * stride < p.rows) issue(s, row + s * stride);
   }
@@ -154,7 +172,7 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
       for (int q = 0; q < P / 2; ++q) {
         float4 g = make_float4(0.f, 0.f, 0.f, 0.f), b = g;
         if (ok[k]) {
-          const int c = tid + THREADS * k;
+          const int c = v0 + 32 * k;
           g = ld_param_f4(p.gamma + c * VEC + 4 * q);
           b = ld_param_f4(p.beta + c * VEC + 4 * q);
         }
@@ -175,49 +193,37 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
 #pragma unroll
       for (int q = 0; q < P; ++q) v[k][q] = dup2(0.f);
 
-    float K;  // the row's shift: its first sum a_0
+    bool timed_out = false;
     const int s = TMA ? static_cast<int>(it % stages) : 0;
     if constexpr (TMA) {
-      // Thread 0 alone waits for the slot's copies; the barrier then releases
-      // the other threads (ordered after its observation of the completed
-      // phase) and tells every thread whether the wait ran out.
-      bool landed = true;
-      if (tid == 0)
-        landed = mbar_wait_bounded(smem_addr(&bars[s]), static_cast<uint32_t>((it / stages) & 1),
-                                   p.wait_limit_ns);
-      if (__syncthreads_or(!landed)) {
-        if (tid == 0) drain_after_timeout(bars, stages, it, row, stride, p.rows);
-        return;
-      }
-      const uint32_t xs = smem0 + s * slot;
-      if (has_r) {
+      // the whole warp waits for its own chunk (one instruction a poll)
+      timed_out = !mbar_wait_bounded(smem_addr(&bars[s * NW + warp]),
+                                     static_cast<uint32_t>((it / stages) & 1), p.wait_limit_ns);
+      if (!timed_out) {
+        const uint32_t xs = smem0 + s * slot;
+        if (has_r) {
 #pragma unroll
-        for (int k = 0; k < NV; ++k)
-          if (ok[k])
-            IO::sum_pairs(ld_shared_v4(xs + (tid + THREADS * k) * 16),
-                          ld_shared_v4(xs + rb + (tid + THREADS * k) * 16), v[k]);
-      } else {
+          for (int k = 0; k < NV; ++k)
+            if (ok[k])
+              IO::sum_pairs(ld_shared_v4(xs + (v0 + 32 * k) * 16),
+                            ld_shared_v4(xs + rb + (v0 + 32 * k) * 16), v[k]);
+        } else {
 #pragma unroll
-        for (int k = 0; k < NV; ++k)
-          if (ok[k]) IO::to_pairs(ld_shared_v4(xs + (tid + THREADS * k) * 16), v[k]);
+          for (int k = 0; k < NV; ++k)
+            if (ok[k]) IO::to_pairs(ld_shared_v4(xs + (v0 + 32 * k) * 16), v[k]);
+        }
       }
-      // a_0 from the staged copy (a broadcast read; unaffected by any global
-      // store, so A may alias R)
-      K = first_sum<DT>(xs, has_r ? xs + rb : 0u);
     } else {
-      // a_0 from global memory, read before the barrier below; every global
-      // store of this row comes after that barrier, so in-place is safe
-      K = has_r ? IO::load1(p.x, base) + IO::load1(p.r, base) : IO::load1(p.x, base);
       const char* xrow = static_cast<const char*>(p.x) + base * S;
       uint4 xv[NV], rv[NV];
 #pragma unroll
       for (int k = 0; k < NV; ++k)
-        if (ok[k]) xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(tid + THREADS * k) * 16);
+        if (ok[k]) xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(v0 + 32 * k) * 16);
       if (has_r) {
         const char* rrow = static_cast<const char*>(p.r) + base * S;
 #pragma unroll
         for (int k = 0; k < NV; ++k)
-          if (ok[k]) rv[k] = ld_stream_v4(rrow + static_cast<int64_t>(tid + THREADS * k) * 16);
+          if (ok[k]) rv[k] = ld_stream_v4(rrow + static_cast<int64_t>(v0 + 32 * k) * 16);
 #pragma unroll
         for (int k = 0; k < NV; ++k)
           if (ok[k]) IO::sum_pairs(xv[k], rv[k], v[k]);
@@ -227,83 +233,85 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
           if (ok[k]) IO::to_pairs(xv[k], v[k]);
       }
     }
-    const float2 negK = dup2(-K);
 
-    // ---- TMA path: A = X + R rounded to the dtype, stored at once; then the
-    // values are shifted in place
-    if constexpr (TMA) {
-      if (p.a != nullptr) {
-        char* arow = static_cast<char*>(p.a) + base * S;
-#pragma unroll
-        for (int k = 0; k < NV; ++k)
-          if (ok[k])
-            st_stream_v4(arow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::from_pairs(v[k]));
-      }
+    // ---- A = X + R rounded to the dtype; each thread writes only what it
+    // read itself, and the shift below comes from registers, so A may alias
+    // X or R
+    if (p.a != nullptr && !timed_out) {
+      char* arow = static_cast<char*>(p.a) + base * S;
 #pragma unroll
       for (int k = 0; k < NV; ++k)
-#pragma unroll
-        for (int q = 0; q < P; ++q) v[k][q] = add2(v[k][q], negK);
+        if (ok[k])
+          st_stream_v4(arow + static_cast<int64_t>(v0 + 32 * k) * 16, IO::from_pairs(v[k]));
     }
 
-    // ---- statistics: per-thread two-pass on the shifted row, warp
-    // butterfly, then the CTA merge of the warp partials
-    Part st = thread_part2<NV, P, FULL, !TMA>(v, ok, negK);
+    // ---- the warp's statistics around its shift K_w (lane 0's first sum)
+    const float Kw = __shfl_sync(0xffffffffu, v[0][0].x, 0);
+    const float2 negK = dup2(-Kw);
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+      for (int q = 0; q < P; ++q) v[k][q] = add2(v[k][q], negK);
+    Part st = thread_part2<NV, P, FULL, false>(v, ok, negK);
     st = butterfly<FULL, 32>(st);
-    Part* rbuf = red + (it & 1) * NW;
-    if (lane == 0) rbuf[warp] = st;
+    WarpPart* rbuf = red + (it & 1) * NW;
+    if (lane == 0) rbuf[warp] = WarpPart{Kw, st.n, st.m, st.M2};
 
+    // ---- all warps' partials in; also the point after which no thread
+    // reads slot s any more
     if constexpr (TMA) {
-      // Also the point after which no thread reads slot s any more.
-      __syncthreads();
-      if (tid == 0) {
+      if (__syncthreads_or(timed_out)) {
+        if (tid == 0) drain_after_timeout(bars, stages, NW, it, row, stride, p.rows);
+        return;
+      }
+      if (lane == 0) {
         const int64_t next = row + stages * stride;
         if (next < p.rows) issue(s, next);
       }
     } else {
       __syncthreads();
-      // the vector path shifts after its A store, which must follow the barrier
-      if (p.a != nullptr) {
-        char* arow = static_cast<char*>(p.a) + base * S;
-#pragma unroll
-        for (int k = 0; k < NV; ++k)
-          if (ok[k])
-            st_stream_v4(arow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::from_pairs(v[k]));
-      }
-#pragma unroll
-      for (int k = 0; k < NV; ++k)
-#pragma unroll
-        for (int q = 0; q < P; ++q) v[k][q] = add2(v[k][q], negK);
     }
 
-    const Part tot = cta_totals<FULL, NW>(rbuf, lane);
+    // ---- CTA merge: every warp's mean moved to warp 0's shift K_0, then
+    // combined (identical totals in every lane)
+    const float K0 = rbuf[0].K;
+    const WarpPart wp = rbuf[lane % NW];
+    Part q;
+    q.n = wp.n;
+    q.m = wp.m + (wp.K - K0);
+    q.M2 = wp.M2;
+    const Part tot = butterfly<FULL, NW>(q);
     const float rstd = row_rstd(tot.M2, p.inv_h, p.eps);
-    const float2 negm = dup2(-tot.m), rstd2 = dup2(rstd);
+    // this warp's values are a - K_w; the row mean is K_0 + m, so
+    // a - mean = (a - K_w) - (m - (K_w - K_0))
+    const float2 negm = dup2(-(tot.m - (Kw - K0))), rstd2 = dup2(rstd);
 
     // ---- normalise + affine from registers, store
     char* yrow = static_cast<char*>(p.y) + base * S;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       if (ok[k]) {
-        const int c = tid + THREADS * k;
+        const int c = v0 + 32 * k;
         float2 o[P];
         if constexpr (RES) {
 #pragma unroll
-          for (int q = 0; q < P; ++q) o[q] = normalise2(v[k][q], negm, rstd2, gr[k][q], br[k][q]);
+          for (int qq = 0; qq < P; ++qq) o[qq] = normalise2(v[k][qq], negm, rstd2, gr[k][qq], br[k][qq]);
         } else {
 #pragma unroll
-          for (int q = 0; q < P / 2; ++q) {
-            const float4 g = ld_param_f4(p.gamma + c * VEC + 4 * q);
-            const float4 b = ld_param_f4(p.beta + c * VEC + 4 * q);
-            o[2 * q] = normalise2(v[k][2 * q], negm, rstd2, make_float2(g.x, g.y), make_float2(b.x, b.y));
-            o[2 * q + 1] =
-                normalise2(v[k][2 * q + 1], negm, rstd2, make_float2(g.z, g.w), make_float2(b.z, b.w));
+          for (int qq = 0; qq < P / 2; ++qq) {
+            const float4 g = ld_param_f4(p.gamma + c * VEC + 4 * qq);
+            const float4 b = ld_param_f4(p.beta + c * VEC + 4 * qq);
+            o[2 * qq] =
+                normalise2(v[k][2 * qq], negm, rstd2, make_float2(g.x, g.y), make_float2(b.x, b.y));
+            o[2 * qq + 1] =
+                normalise2(v[k][2 * qq + 1], negm, rstd2, make_float2(g.z, g.w), make_float2(b.z, b.w));
           }
         }
         st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::from_pairs(o));
       }
     }
     if (tid == 0) {
-      if (p.mean != nullptr) p.mean[row] = K + tot.m;
+      if (p.mean != nullptr) p.mean[row] = K0 + tot.m;
       if (p.rstd != nullptr) p.rstd[row] = rstd;
     }
   }
@@ -426,7 +434,7 @@ int launch_row_t(const RowArgs& p, const LaunchCtx& c) {
   const uint32_t row_bytes = static_cast<uint32_t>(p.H) * S;
   const uint32_t rb = (row_bytes + 127u) & ~127u;
   const uint32_t slot = p.r ? 2u * rb : rb;
-  const uint32_t extra = 8u * kMaxStages + 2u * (THREADS / 32) * sizeof(Part);
+  const uint32_t extra = 8u * kMaxStages * (THREADS / 32) + 2u * (THREADS / 32) * sizeof(WarpPart);
   const void* f = reinterpret_cast<const void*>(&k_cta_row<DT, THREADS, NV, TMA, FULL>);
   int stages = 0, per_sm = 0;
   uint32_t smem = extra;
@@ -495,7 +503,6 @@ int launch_row_dispatch(const RowArgs& p, const LaunchCtx& c, const char** name)
   if (c.cta_threads != 0) {
     // Tuning shapes (TMA staging of 16-bit rows only); otherwise by H below.
     if constexpr (TMA && VEC == 8) {
-      if (c.cta_threads == 64 && nvec <= 64 * 8) { *name = "cta_tma_t64_nv8"; return launch_row<DT, 64, 8, true>(p, c); }
       if (c.cta_threads == 128 && nvec <= 128 * 4) { *name = "cta_tma_t128_nv4"; return launch_row<DT, 128, 4, true>(p, c); }
       if (c.cta_threads == 256 && nvec <= 256 * 2) { *name = "cta_tma_t256_nv2"; return launch_row<DT, 256, 2, true>(p, c); }
       if (c.cta_threads == 512 && nvec <= 512 * 1) { *name = "cta_tma_t512_nv1"; return launch_row<DT, 512, 1, true>(p, c); }

@@ -383,8 +383,8 @@ def test_dependent_chain_keeps_order_under_pdl(name):
     check(w, x0, out, f"{name} chain step 0")
 
 
-@pytest.mark.parametrize("threads", [64, 128, 256, 512])
-@pytest.mark.parametrize("stages", [1, 2, 3])
+@pytest.mark.parametrize("threads", [128, 256, 512])
+@pytest.mark.parametrize("stages", [1, 2, 3, 4])
 def test_tma_tuning_shapes(threads, stages):
     w = synth.with_rows(synth.get("pages_2048x4096_fp16"), 150)
     d = synth.make_inputs(w, seed=13)
