@@ -332,11 +332,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // ------------------------------------------------------------- statistics
-// Every thread of a row works on the row's values shifted by one common
-// value K of that row (its first sum a_0): Chan, Golub and LeVeque's
-// "shifted data".  The sums then run at the size of the row's spread, so a
-// row whose mean is large against its standard deviation loses nothing to
-// the mean's magnitude, and a constant row gives exactly m = 0, M2 = 0.
+// Threads work on the row's values shifted by a value K of that row (the
+// row's first sum in the warp kernels, the first sum of a warp's chunk in the
+// CTA kernel): Chan, Golub and LeVeque's "shifted data".  The sums then run
+// at the size of the row's spread, so a row whose mean is large against its
+// standard deviation loses nothing to the mean's magnitude, and a constant
+// row gives exactly m = 0, M2 = 0.
 //
 // A partial covers n of the row's values: m = mean of (a - K), M2 = sum of
 // squared deviations from that mean.

@@ -3,13 +3,14 @@
 // The grid is persistent (one wave of resident CTAs, sized from the SM count
 // and the occupancy the kernel reaches); CTA b takes rows b, b + grid, ...
 //
-// TMA variant: thread 0 stages whole rows of X and R into shared memory with
-// one-dimensional bulk copies (cp.async.bulk, completion counted on an
-// mbarrier) into a ring of `stages` slots: the first `stages` rows are
-// requested at once, and a slot is refilled with the CTA's row `stages`
-// ahead as soon as every thread has moved the slot's row into registers.
-// The reduction and the normalisation both run on those registers, and Y / A
-// go straight to global memory with 16-byte streaming stores.  When a thread
+// TMA variant: each warp stages its own chunk of every row of X and R into
+// shared memory with one-dimensional bulk copies (cp.async.bulk, completion
+// counted on the warp's mbarrier) into a ring of `stages` slots: the first
+// `stages` rows are requested at once, and a slot is refilled with the CTA's
+// row `stages` ahead as soon as every thread has moved the slot's row into
+// registers.  The reduction and the normalisation both run on those
+// registers, and Y / A go straight to global memory with 16-byte streaming
+// stores.  When a thread
 // holds at most 32 values, it also keeps gamma and beta of its columns in
 // registers for the CTA's lifetime: reloading them for every row (8 bytes a
 // column, twice the row's own 16-bit X and R) would make the L1 data path,
