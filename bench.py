@@ -779,6 +779,7 @@ def run_backward(args):
         mba.add_layernorm_bwd(s["dy"], s["a"], s["mean"], s["rstd"], gamma, s["dx"], s["dg"],
                               s["db"], workspace=s["ws"])
 
+    mba.addln_set_cta_shape(0, args.stages)   # staging ring depth (tuning; 0 = default)
     step(0)
     torch.cuda.synchronize()
     path = mba.addln_last_path()
@@ -791,6 +792,7 @@ def run_backward(args):
     W = max(3, args.warmup)
     graph_steps = args.graph_steps or max(n_sets, min(K, 256))
     elapsed, _, _ = timed_graph_run(step, K, W, n_sets, graph_steps, lambda: None)
+    mba.addln_set_cta_shape(0, 0)
     if mba.addln_get_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
     alg = bwd_algorithmic_bytes(w)

@@ -362,7 +362,7 @@ int add_layernorm_bwd(const void* dy, const void* a, const float* mean, const fl
   c.grid_cap = 0;
   c.pdl = g_pdl.load(std::memory_order_relaxed) != 0;
   c.cta_threads = 0;
-  c.stages = 0;
+  c.stages = g_stages.load(std::memory_order_relaxed);  // ring depth (tuning knob)
   const int rc = device_info(&c.dev);
   if (rc != ADDLN_OK) return rc;
   const int64_t row_bytes = H * elem_bytes(dtype);

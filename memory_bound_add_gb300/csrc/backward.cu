@@ -60,114 +60,16 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// --------------------------------------------------------- warp per row
-constexpr int kWarps = 4;
-
-template <int DT, int NV, bool FULL>
-__global__ void __launch_bounds__(kWarps * 32, 3) k_bwd_warp(const BwdArgs p) {
-  using IO = Io<DT>;
-  constexpr int VEC = IO::kVec;
-  constexpr int S = IO::kBytes;
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = p.H;
-  const int nvec = H / VEC;
-  const bool cols = p.ws != nullptr;
-  // this warp's partials, lane-major so a warp's accesses hit 32 distinct
-  // banks: column (lane + 32 k) * VEC + i lives at slot (k * VEC + i) * 32 + lane
-  // of the dgamma half [0, 32 NV VEC) and of the dbeta half after it
-  constexpr int kHalf = 32 * NV * VEC;
-  float* part = reinterpret_cast<float*>(smem) + warp * 2 * kHalf;
-
-  bool ok[NV];
-#pragma unroll
-  for (int k = 0; k < NV; ++k) ok[k] = FULL || (lane + 32 * k) < nvec;
-  if (cols)
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        part[(k * VEC + e) * 32 + lane] = 0.f;
-        part[kHalf + (k * VEC + e) * 32 + lane] = 0.f;
-      }
-  pdl_trigger();
-  pdl_wait();
-
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp; row < p.rows;
-       row += static_cast<int64_t>(gridDim.x) * kWarps) {
-    const int64_t boff = row * static_cast<int64_t>(H) * S;
-    uint4 dv[NV], av[NV], rv[NV];
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-      if (ok[k]) {
-        dv[k] = ld_stream_v4(static_cast<const char*>(p.dy) + boff + (lane + 32 * k) * 16);
-        av[k] = ld_stream_v4(static_cast<const char*>(p.a) + boff + (lane + 32 * k) * 16);
-      }
-    if (p.dres != nullptr)
-#pragma unroll
-      for (int k = 0; k < NV; ++k)
-        if (ok[k]) rv[k] = ld_stream_v4(static_cast<const char*>(p.dres) + boff + (lane + 32 * k) * 16);
-    const float mu = __ldg(p.mean + row), rs = __ldg(p.rstd + row);
-    float xh[NV][VEC];  // dY stays packed in dv; g = dY * gamma is formed twice
-    float sg = 0.f, sgx = 0.f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      if (ok[k]) {
-        const int c = lane + 32 * k;
-        float d[VEC], gg[VEC];
-        IO::unpack(dv[k], d);
-        IO::unpack(av[k], xh[k]);
-        load_gamma<VEC>(p.gamma + c * VEC, gg);
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-          xh[k][i] = (xh[k][i] - mu) * rs;
-          const float g = d[i] * gg[i];
-          sg += g;
-          sgx = fmaf(g, xh[k][i], sgx);
-        }
-        if (cols)
-#pragma unroll
-          for (int i = 0; i < VEC; ++i) {
-            float* sl = part + (k * VEC + i) * 32 + lane;
-            sl[0] = fmaf(d[i], xh[k][i], sl[0]);
-            sl[kHalf] += d[i];
-          }
-      }
-    }
-    sg = warp_sum(sg);
-    sgx = warp_sum(sgx);
-    const float mg = sg * p.inv_h, mgx = sgx * p.inv_h;
-    char* drow = static_cast<char*>(p.dx) + boff;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      if (ok[k]) {
-        const int c = lane + 32 * k;
-        float d[VEC], gg[VEC], o[VEC], rr[VEC];
-        IO::unpack(dv[k], d);
-        load_gamma<VEC>(p.gamma + c * VEC, gg);
-        if (p.dres != nullptr) IO::unpack(rv[k], rr);
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-          o[i] = rs * (d[i] * gg[i] - fmaf(xh[k][i], mgx, mg));
-          if (p.dres != nullptr) o[i] += rr[i];
-        }
-        st_stream_v4(drow + c * 16, IO::pack(o));
-      }
-    }
-  }
-  if (cols) {
-    __syncthreads();
-    const float* all = reinterpret_cast<const float*>(smem);
-    float* out = p.ws + static_cast<int64_t>(blockIdx.x) * 2 * H;
-    for (int j = tid; j < 2 * H; j += kWarps * 32) {
-      const int half = j < H ? 0 : 1, col = j - half * H;
-      const int c = col / VEC, i = col - c * VEC;
-      const int slot = half * kHalf + ((c >> 5) * VEC + i) * 32 + (c & 31);
-      float s = all[slot];
-#pragma unroll
-      for (int w = 1; w < kWarps; ++w) s += all[w * 2 * kHalf + slot];
-      out[j] = s;
-    }
+// After a wait of warp w ran out: waits (bounded) for that warp's copies
+// still in flight -- rows it .. it+stages-1 of its ring -- so that none lands
+// in shared memory the next CTA on this SM may reuse.
+__device__ __noinline__ void drain_res(uint64_t* bars, int stages, int nw, int w, int64_t it,
+                                       int64_t row, int64_t stride, int64_t rows) {
+  for (int j = 0; j < stages; ++j) {
+    const int64_t itj = it + j;
+    if (row + j * stride < rows)
+      mbar_wait_bounded(smem_addr(&bars[(itj % stages) * nw + w]),
+                        static_cast<uint32_t>((itj / stages) & 1), 1000000000ull);
   }
 }
 
@@ -309,6 +211,242 @@ __global__ void __launch_bounds__(THREADS) k_bwd_cta(const BwdArgs p) {
   }
 }
 
+// ------------------------------------- register-resident column sums
+// The main backward kernels.  gamma and the thread's dgamma / dbeta
+// accumulators stay in registers for the CTA's lifetime (so per row the L1
+// data path sees only the staged dY and A and the dX stores; keeping the
+// partials in shared memory cost four shared accesses an element and reading
+// gamma twice a row another two 16-byte loads per 4 columns, which made L1,
+// not HBM, the limit), values are held as fp32 pairs, and dY and A arrive by
+// bulk copies into a per-warp ring of `stages` slots (each warp's own
+// mbarriers), refilled as soon as the warp is past a slot.
+//
+// ROWWARP: each warp owns whole rows (lanes take vectors lane + 32 k) and
+// reduces with shuffles alone; at the end the CTA adds its warps'
+// accumulators in warp order into its [2][H] partial.  Otherwise the CTA owns
+// a row and warp w the contiguous chunk of vectors [w CV, (w+1) CV); the two
+// row sums go through shared memory and one barrier, and every thread writes
+// its own columns of the CTA's partial.
+constexpr int kMaxStagesRes = 4;
+
+template <int DT, int THREADS, int NV, bool ROWWARP>
+constexpr int bwd_res_regs() {
+  return ROWWARP ? 168 : 128;
+}
+
+template <int DT, int THREADS, int NV, bool FULL, bool ROWWARP>
+__global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS, NV, ROWWARP>()))
+    k_bwd_res(const BwdArgs p, const int stages) {
+  using IO = Io<DT>;
+  constexpr int VEC = IO::kVec;
+  constexpr int P = VEC / 2;
+  constexpr int S = IO::kBytes;
+  constexpr int NW = THREADS / 32;
+  constexpr int CV = 32 * NV;                 // vectors a warp stages per row
+  constexpr uint32_t kRegion = 2u * CV * 16u;  // a warp's slot: dY chunk, then A chunk
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H = p.H;
+  const int nvec = H / VEC;
+  const bool cols = p.ws != nullptr;
+  const uint32_t row_bytes = static_cast<uint32_t>(H) * S;
+  const uint32_t ring = static_cast<uint32_t>(stages) * NW * kRegion;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring);  // [stages][NW]
+  float2* red = reinterpret_cast<float2*>(smem + ring + 8u * kMaxStagesRes * NW);  // [2][NW]
+  const uint32_t smem0 = smem_addr(smem);
+
+  const int v0 = ROWWARP ? lane : warp * CV + lane;
+  bool ok[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) ok[k] = FULL || v0 + 32 * k < nvec;
+  const int cvecs = ROWWARP ? nvec : (FULL ? CV : min(CV, max(0, nvec - warp * CV)));
+  const uint32_t chunk_bytes = static_cast<uint32_t>(cvecs) * 16u;
+  const uint32_t chunk_off = ROWWARP ? 0u : static_cast<uint32_t>(warp * CV) * 16u;
+
+  const int64_t stride = ROWWARP ? static_cast<int64_t>(gridDim.x) * NW : gridDim.x;
+  int64_t row = ROWWARP ? static_cast<int64_t>(blockIdx.x) * NW + warp : blockIdx.x;
+
+  if (tid == 0) {
+    for (int i = 0; i < stages * NW; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint64_t policy = policy_evict_first();
+  pdl_trigger();
+  pdl_wait();
+
+  auto region = [&](int s) { return smem0 + static_cast<uint32_t>(s * NW + warp) * kRegion; };
+  auto issue = [&](int s, int64_t rr) {  // lane 0: the warp's chunk of row rr into slot s
+    const uint32_t bar = smem_addr(&bars[s * NW + warp]);
+    mbar_arrive_expect_tx(bar, 2u * chunk_bytes);
+    if (chunk_bytes != 0) {
+      const int64_t off = rr * static_cast<int64_t>(row_bytes) + chunk_off;
+      bulk_g2s(region(s), static_cast<const char*>(p.dy) + off, chunk_bytes, bar, policy);
+      bulk_g2s(region(s) + CV * 16u, static_cast<const char*>(p.a) + off, chunk_bytes, bar, policy);
+    }
+  };
+  if (lane == 0)
+    for (int s = 0; s < stages; ++s)
+      if (row + s * stride < p.rows) issue(s, row + s * stride);
+
+  float2 gam[NV][P], dg[NV][P], db[NV][P];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+#pragma unroll
+    for (int q = 0; q < P / 2; ++q) {
+      float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok[k]) g = ld_param_f4(p.gamma + (v0 + 32 * k) * VEC + 4 * q);
+      gam[k][2 * q] = make_float2(g.x, g.y);
+      gam[k][2 * q + 1] = make_float2(g.z, g.w);
+    }
+#pragma unroll
+    for (int q = 0; q < P; ++q) dg[k][q] = db[k][q] = dup2(0.f);
+  }
+
+  bool failed = false;
+  for (int64_t it = 0; row < p.rows; ++it, row += stride) {
+    const int s = static_cast<int>(it % stages);
+    // warp-uniform: every lane polls the warp's barrier with its own clock
+    const bool timed_out = __any_sync(
+        0xffffffffu, !mbar_wait_bounded(smem_addr(&bars[s * NW + warp]),
+                                        static_cast<uint32_t>((it / stages) & 1), p.wait_limit_ns));
+    const float mu = __ldg(p.mean + row), rs = __ldg(p.rstd + row);
+    const float2 negmu = dup2(-mu), rs2 = dup2(rs);
+    // The CTA form keeps dY (packed) and xhat in registers across the row
+    // sums; the warp form, holding twice the columns, reads both again from
+    // its slot, which it refills only after the row is done.
+    constexpr int KEEP = ROWWARP ? 1 : NV;
+    uint4 dv[KEEP];
+    float2 xh[KEEP][P];
+    float2 sg2 = dup2(0.f), sgx2 = dup2(0.f);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int kk = ROWWARP ? 0 : k;
+      dv[kk] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int q = 0; q < P; ++q) xh[kk][q] = dup2(0.f);
+      if (ok[k] && !timed_out) {
+        dv[kk] = ld_shared_v4(region(s) + (32 * k + lane) * 16);
+        IO::to_pairs(ld_shared_v4(region(s) + CV * 16u + (32 * k + lane) * 16), xh[kk]);
+        float2 d[P];
+        IO::to_pairs(dv[kk], d);
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          xh[kk][q] = mul2(add2(xh[kk][q], negmu), rs2);
+          const float2 g = mul2(d[q], gam[k][q]);
+          sg2 = add2(sg2, g);
+          sgx2 = fma2(g, xh[kk][q], sgx2);
+          if (cols) {
+            dg[k][q] = fma2(d[q], xh[kk][q], dg[k][q]);
+            db[k][q] = add2(db[k][q], d[q]);
+          }
+        }
+      }
+    }
+    float tg = warp_sum(sg2.x + sg2.y), tgx = warp_sum(sgx2.x + sgx2.y);
+    if constexpr (ROWWARP) {
+      if (timed_out) {
+        if (lane == 0) drain_res(bars, stages, NW, warp, it, row, stride, p.rows);
+        failed = true;
+        break;
+      }
+    } else {
+      float2* rbuf = red + (it & 1) * NW;
+      if (lane == 0) rbuf[warp] = make_float2(tg, tgx);
+      if (__syncthreads_or(timed_out)) {
+        if (tid == 0)
+          for (int w = 0; w < NW; ++w) drain_res(bars, stages, NW, w, it, row, stride, p.rows);
+        failed = true;
+        break;
+      }
+      if (lane == 0 && row + stages * stride < p.rows) issue(s, row + stages * stride);
+      tg = 0.f;
+      tgx = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        tg += rbuf[w].x;
+        tgx += rbuf[w].y;
+      }
+    }
+    // dA = rstd * (g - (xhat * mean(g xhat) + mean(g))) (+ dA_in)
+    const float2 nmgx = dup2(-(tgx * p.inv_h)), nmg = dup2(-(tg * p.inv_h));
+    char* drow = static_cast<char*>(p.dx) + row * static_cast<int64_t>(row_bytes);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (ok[k]) {
+        const int c = v0 + 32 * k;
+        float2 d[P], o[P], rr[P], x[P];
+        if constexpr (ROWWARP) {
+          IO::to_pairs(ld_shared_v4(region(s) + (32 * k + lane) * 16), d);
+          IO::to_pairs(ld_shared_v4(region(s) + CV * 16u + (32 * k + lane) * 16), x);
+#pragma unroll
+          for (int q = 0; q < P; ++q) x[q] = mul2(add2(x[q], negmu), rs2);
+        } else {
+          IO::to_pairs(dv[k], d);
+#pragma unroll
+          for (int q = 0; q < P; ++q) x[q] = xh[k][q];
+        }
+        if (p.dres != nullptr)
+          IO::to_pairs(ld_stream_v4(static_cast<const char*>(p.dres) +
+                                    row * static_cast<int64_t>(row_bytes) + c * 16),
+                       rr);
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          o[q] = mul2(rs2, add2(mul2(d[q], gam[k][q]), fma2(x[q], nmgx, nmg)));
+          if (p.dres != nullptr) o[q] = add2(o[q], rr[q]);
+        }
+        st_stream_v4(drow + static_cast<int64_t>(c) * 16, IO::from_pairs(o));
+      }
+    }
+    if constexpr (ROWWARP) {
+      __syncwarp();  // every lane is past slot s
+      if (lane == 0 && row + stages * stride < p.rows) issue(s, row + stages * stride);
+    }
+  }
+  if (failed) atomicExch(&g_bwd_error, ADDLN_ERR_DEVICE_TIMEOUT);
+  if (!cols) return;
+
+  if constexpr (ROWWARP) {
+    // warps' accumulators into shared memory (the ring is free now), then
+    // summed in warp order into the CTA's partial
+    __syncthreads();
+    float* part = reinterpret_cast<float*>(smem);  // [NW][2][H]
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (ok[k])
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          const int j = (v0 + 32 * k) * VEC + 2 * q;
+          float* w0 = part + static_cast<int64_t>(warp) * 2 * H;
+          w0[j] = dg[k][q].x;
+          w0[j + 1] = dg[k][q].y;
+          w0[H + j] = db[k][q].x;
+          w0[H + j + 1] = db[k][q].y;
+        }
+    __syncthreads();
+    float* out = p.ws + static_cast<int64_t>(blockIdx.x) * 2 * H;
+    for (int j = tid; j < 2 * H; j += THREADS) {
+      float t = part[j];
+#pragma unroll
+      for (int w = 1; w < NW; ++w) t += part[static_cast<int64_t>(w) * 2 * H + j];
+      out[j] = t;
+    }
+  } else {
+    float* out = p.ws + static_cast<int64_t>(blockIdx.x) * 2 * H;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (ok[k])
+#pragma unroll
+        for (int q = 0; q < P / 2; ++q) {
+          const int j = (v0 + 32 * k) * VEC + 4 * q;
+          *reinterpret_cast<float4*>(out + j) =
+              make_float4(dg[k][2 * q].x, dg[k][2 * q].y, dg[k][2 * q + 1].x, dg[k][2 * q + 1].y);
+          *reinterpret_cast<float4*>(out + H + j) =
+              make_float4(db[k][2 * q].x, db[k][2 * q].y, db[k][2 * q + 1].x, db[k][2 * q + 1].y);
+        }
+  }
+}
+
 // ------------------------------------------------ CTA per row, elements
 template <int DT, int THREADS>
 __global__ void __launch_bounds__(THREADS) k_bwd_scalar(const BwdArgs p) {
@@ -371,29 +509,38 @@ __global__ void __launch_bounds__(THREADS) k_bwd_scalar(const BwdArgs p) {
 }
 
 // dgamma_j = sum_b ws[b][0][j], dbeta_j = sum_b ws[b][1][j].  A block covers
-// 32 columns with 8 slices of the partials each (slice s takes b = s, s + 8,
-// ...); the 8 slice sums are then added in slice order, so the result does
-// not depend on scheduling.
-constexpr int kColCols = 32, kColSlices = 8;
+// 32 columns with 16 slices of the partials (slice s takes b = s, s + 16,
+// ...; a warp reads 32 adjacent columns of one partial, 128 coalesced
+// bytes); each thread keeps four accumulators over interleaved subsequences
+// of its slice, so four loads are in flight, then adds them in a fixed
+// order; the 16 slice sums are added in slice order.  The result does not
+// depend on scheduling.
+constexpr int kColCols = 32, kColSlices = 16, kColAcc = 4;
 
-__global__ void __launch_bounds__(kColCols * kColSlices) k_colsum(const float* ws, int64_t G, int H,
-                                                                  float* dgamma, float* dbeta) {
-  __shared__ float part[kColSlices][kColCols];
+__global__ void __launch_bounds__(kColCols * kColSlices, 2) k_colsum(const float* ws, int64_t G, int H,
+                                                                     float* dgamma, float* dbeta) {
+  __shared__ float part[kColSlices][kColCols + 1];
   pdl_trigger();
   pdl_wait();
   const int lc = threadIdx.x % kColCols, sl = threadIdx.x / kColCols;
   const int j = blockIdx.x * kColCols + lc;
   const int64_t ld = 2 * static_cast<int64_t>(H);
-  float s = 0.f;
+  float acc[kColAcc] = {0.f, 0.f, 0.f, 0.f};
   if (j < 2 * H) {
-#pragma unroll 4
-    for (int64_t b = sl; b < G; b += kColSlices) s += ws[b * ld + j];
+    constexpr int64_t kStep = static_cast<int64_t>(kColSlices) * kColAcc;
+    for (int64_t b = sl; b < G; b += kStep) {
+#pragma unroll
+      for (int u = 0; u < kColAcc; ++u) {
+        const int64_t bu = b + static_cast<int64_t>(u) * kColSlices;
+        if (bu < G) acc[u] += ws[bu * ld + j];
+      }
+    }
   }
-  part[sl][lc] = s;
+  part[sl][lc] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
   __syncthreads();
   if (sl == 0 && j < 2 * H) {
     float t = part[0][lc];
-#pragma unroll
+#pragma unroll 8
     for (int q = 1; q < kColSlices; ++q) t += part[q][lc];
     if (j < H)
       dgamma[j] = t;
@@ -444,7 +591,8 @@ struct Plan {
   int threads = 0;
   uint32_t smem = 0;
   int64_t grid = 0;  // also the number of workspace partials
-  int kind = 0;      // 0 warp, 1 cta, 2 scalar
+  int kind = 0;      // 0 warp, 1 cta, 2 scalar, 3 register-resident (takes `stages`)
+  int stages = 0;
   const char* name = "none";
 };
 
@@ -460,19 +608,6 @@ int64_t grid_of(int64_t rows, int64_t per_cta_rows, int per_sm, const DeviceInfo
   return g < 1 ? 1 : g;
 }
 
-template <int DT, int NV, bool FULL>
-int plan_warp(const BwdArgs& p, const DeviceInfo& dev, Plan* pl) {
-  pl->f = reinterpret_cast<const void*>(&k_bwd_warp<DT, NV, FULL>);
-  pl->threads = kWarps * 32;
-  pl->smem = kWarps * 2u * 32u * NV * Io<DT>::kVec * 4u;
-  const int per_sm = resident(pl->f, pl->threads, static_cast<int>(pl->smem), dev);
-  if (per_sm < 0) return ADDLN_ERR_CUDA;
-  if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
-  pl->grid = grid_of(p.rows, kWarps, per_sm, dev);
-  pl->kind = 0;
-  return ADDLN_OK;
-}
-
 template <int DT, int THREADS, int NV, bool FULL>
 int plan_cta(const BwdArgs& p, const DeviceInfo& dev, Plan* pl) {
   const uint32_t row_bytes = static_cast<uint32_t>(p.H) * Io<DT>::kBytes;
@@ -486,6 +621,39 @@ int plan_cta(const BwdArgs& p, const DeviceInfo& dev, Plan* pl) {
   if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
   pl->grid = grid_of(p.rows, 1, per_sm, dev);
   pl->kind = 1;
+  return ADDLN_OK;
+}
+
+// Register-resident kernel: two ring slots a warp by default (three for the
+// warp-per-row form, which holds a slot for its whole row); the slot knob
+// (1..4) changes only the launch's slots, never its grid, so the workspace
+// size does not depend on it.  The warp-per-row form keeps at least two
+// slots, whose space its final per-warp column sums reuse.
+template <int DT, int THREADS, int NV, bool FULL, bool ROWWARP>
+int plan_res(const BwdArgs& p, const DeviceInfo& dev, int stages_knob, Plan* pl) {
+  constexpr int NW = THREADS / 32;
+  constexpr uint32_t region = 2u * 32u * NV * 16u;
+  constexpr int kDefaultStages = ROWWARP ? 3 : 2;
+  auto smem_of = [](int st) {
+    return static_cast<uint32_t>(st) * NW * region + 8u * kMaxStagesRes * NW + 2u * NW * 8u;
+  };
+  int st = stages_knob > 0 ? stages_knob : kDefaultStages;
+  if (ROWWARP && st < 2) st = 2;
+  if (st > kMaxStagesRes) return ADDLN_ERR_UNSUPPORTED;
+  pl->f = reinterpret_cast<const void*>(&k_bwd_res<DT, THREADS, NV, FULL, ROWWARP>);
+  pl->threads = THREADS;
+  pl->stages = st;
+  pl->smem = smem_of(st);
+  if (pl->smem > static_cast<uint32_t>(dev.smem_optin) ||
+      smem_of(kDefaultStages) > static_cast<uint32_t>(dev.smem_optin))
+    return ADDLN_ERR_UNSUPPORTED;
+  const int per_sm = resident(pl->f, THREADS, static_cast<int>(smem_of(kDefaultStages)), dev);
+  if (per_sm < 0) return ADDLN_ERR_CUDA;
+  if (per_sm == 0) return ADDLN_ERR_UNSUPPORTED;
+  if (st != kDefaultStages && resident(pl->f, THREADS, static_cast<int>(pl->smem), dev) <= 0)
+    return ADDLN_ERR_UNSUPPORTED;
+  pl->grid = grid_of(p.rows, ROWWARP ? NW : 1, per_sm, dev);
+  pl->kind = 3;
   return ADDLN_OK;
 }
 
@@ -505,20 +673,28 @@ int plan_scalar(const BwdArgs& p, const DeviceInfo& dev, Plan* pl) {
 }
 
 template <int DT>
-int plan_dt(const BwdArgs& p, bool vec_ok, const DeviceInfo& dev, Plan* pl) {
+int plan_dt(const BwdArgs& p, bool vec_ok, const DeviceInfo& dev, int stages_knob, Plan* pl) {
   constexpr int VEC = Io<DT>::kVec;
   const int nvec = p.H / VEC;
   if (vec_ok && p.H <= 1024) {
+    // a warp per row, 128-thread CTAs
     const int nv = (nvec + 31) / 32;
-    if (nv <= 1) { pl->name = "bwd_warp_nv1"; return nvec == 32 ? plan_warp<DT, 1, true>(p, dev, pl) : plan_warp<DT, 1, false>(p, dev, pl); }
-    if (nv <= 2) { pl->name = "bwd_warp_nv2"; return nvec == 64 ? plan_warp<DT, 2, true>(p, dev, pl) : plan_warp<DT, 2, false>(p, dev, pl); }
-    if (nv <= 4) { pl->name = "bwd_warp_nv4"; return nvec == 128 ? plan_warp<DT, 4, true>(p, dev, pl) : plan_warp<DT, 4, false>(p, dev, pl); }
+    if (nv <= 1) { pl->name = "bwd_res_warp_nv1"; return nvec == 32 ? plan_res<DT, 128, 1, true, true>(p, dev, stages_knob, pl) : plan_res<DT, 128, 1, false, true>(p, dev, stages_knob, pl); }
+    if (nv <= 2) { pl->name = "bwd_res_warp_nv2"; return nvec == 64 ? plan_res<DT, 128, 2, true, true>(p, dev, stages_knob, pl) : plan_res<DT, 128, 2, false, true>(p, dev, stages_knob, pl); }
+    if (nv <= 3) { pl->name = "bwd_res_warp_nv3"; return nvec == 96 ? plan_res<DT, 128, 3, true, true>(p, dev, stages_knob, pl) : plan_res<DT, 128, 3, false, true>(p, dev, stages_knob, pl); }
+    if (nv <= 4) { pl->name = "bwd_res_warp_nv4"; return nvec == 128 ? plan_res<DT, 128, 4, true, true>(p, dev, stages_knob, pl) : plan_res<DT, 128, 4, false, true>(p, dev, stages_knob, pl); }
     if constexpr (VEC == 4)
-      if (nv <= 8) { pl->name = "bwd_warp_nv8"; return nvec == 256 ? plan_warp<DT, 8, true>(p, dev, pl) : plan_warp<DT, 8, false>(p, dev, pl); }
+      if (nv <= 8) { pl->name = "bwd_res_warp_nv8"; return nvec == 256 ? plan_res<DT, 128, 8, true, true>(p, dev, stages_knob, pl) : plan_res<DT, 128, 8, false, true>(p, dev, stages_knob, pl); }
   }
   if (vec_ok && p.H > 1024) {
-    if (nvec <= 128 * 4) { pl->name = "bwd_cta_tma_t128_nv4"; return nvec == 512 ? plan_cta<DT, 128, 4, true>(p, dev, pl) : plan_cta<DT, 128, 4, false>(p, dev, pl); }
-    if (nvec <= 256 * 4) { pl->name = "bwd_cta_tma_t256_nv4"; return nvec == 1024 ? plan_cta<DT, 256, 4, true>(p, dev, pl) : plan_cta<DT, 256, 4, false>(p, dev, pl); }
+    // a CTA per row, 16 columns a thread
+    constexpr int NVR = 16 / VEC;
+    if (nvec <= 128 * NVR) { pl->name = "bwd_res_cta_t128"; return nvec == 128 * NVR ? plan_res<DT, 128, NVR, true, false>(p, dev, stages_knob, pl) : plan_res<DT, 128, NVR, false, false>(p, dev, stages_knob, pl); }
+    if (nvec <= 256 * NVR) { pl->name = "bwd_res_cta_t256"; return nvec == 256 * NVR ? plan_res<DT, 256, NVR, true, false>(p, dev, stages_knob, pl) : plan_res<DT, 256, NVR, false, false>(p, dev, stages_knob, pl); }
+    if (nvec <= 512 * NVR) { pl->name = "bwd_res_cta_t512"; return nvec == 512 * NVR ? plan_res<DT, 512, NVR, true, false>(p, dev, stages_knob, pl) : plan_res<DT, 512, NVR, false, false>(p, dev, stages_knob, pl); }
+  }
+  if (vec_ok && p.H > 1024) {
+    // longer 16-bit rows: column partials in shared memory
     if (nvec <= 512 * 4) { pl->name = "bwd_cta_tma_t512_nv4"; return nvec == 2048 ? plan_cta<DT, 512, 4, true>(p, dev, pl) : plan_cta<DT, 512, 4, false>(p, dev, pl); }
   }
   pl->name = "bwd_cta_scalar_t512";
@@ -529,13 +705,13 @@ int plan_dt(const BwdArgs& p, bool vec_ok, const DeviceInfo& dev, Plan* pl) {
 
 // Chooses the row kernel; *partials = the number of [2][H] fp32 workspace
 // partials its grid writes.
-int plan_bwd(int dtype, const BwdArgs& p, bool vec_ok, const DeviceInfo& dev, int64_t* partials,
-             const char** name, Plan* out) {
+int plan_bwd(int dtype, const BwdArgs& p, bool vec_ok, const DeviceInfo& dev, int stages_knob,
+             int64_t* partials, const char** name, Plan* out) {
   int rc;
   switch (dtype) {
-    case kF32: rc = plan_dt<kF32>(p, vec_ok, dev, out); break;
-    case kF16: rc = plan_dt<kF16>(p, vec_ok, dev, out); break;
-    case kBF16: rc = plan_dt<kBF16>(p, vec_ok, dev, out); break;
+    case kF32: rc = plan_dt<kF32>(p, vec_ok, dev, stages_knob, out); break;
+    case kF16: rc = plan_dt<kF16>(p, vec_ok, dev, stages_knob, out); break;
+    case kBF16: rc = plan_dt<kBF16>(p, vec_ok, dev, stages_knob, out); break;
     default: return ADDLN_ERR_DTYPE;
   }
   if (rc == ADDLN_OK) {
@@ -554,7 +730,7 @@ int64_t bwd_workspace_bytes(int dtype, int64_t rows, int64_t H, bool vec_ok, con
   bw::Plan pl;
   int64_t partials = 0;
   const char* name = nullptr;
-  const int rc = bw::plan_bwd(dtype, p, vec_ok, dev, &partials, &name, &pl);
+  const int rc = bw::plan_bwd(dtype, p, vec_ok, dev, 0, &partials, &name, &pl);
   if (rc != ADDLN_OK) return rc;
   return partials * 2 * H * 4;
 }
@@ -567,7 +743,7 @@ int launch_bwd(int dtype, const void* dy, const void* a, const float* mean, cons
                 static_cast<float>(1.0 / static_cast<double>(H)), wait_limit_ns};
   bw::Plan pl;
   int64_t partials = 0;
-  int rc = bw::plan_bwd(dtype, p, vec_ok, c.dev, &partials, name, &pl);
+  int rc = bw::plan_bwd(dtype, p, vec_ok, c.dev, c.stages, &partials, name, &pl);
   if (rc != ADDLN_OK) return rc;
   const bool want_cols = dgamma != nullptr;
   if (want_cols) {
@@ -575,10 +751,17 @@ int launch_bwd(int dtype, const void* dy, const void* a, const float* mean, cons
       return ADDLN_ERR_WORKSPACE;
     p.ws = static_cast<float*>(ws);
   }
-  // every row kernel has the signature void(BwdArgs)
-  auto kernel = reinterpret_cast<void (*)(bw::BwdArgs)>(const_cast<void*>(pl.f));
-  cudaError_t e = launch_kernel(kernel, dim3(static_cast<unsigned>(pl.grid)), dim3(pl.threads),
-                                pl.smem, c.stream, c.pdl, p);
+  // the register-resident kernels take (BwdArgs, stages), the others (BwdArgs)
+  cudaError_t e;
+  if (pl.kind == 3) {
+    auto kernel = reinterpret_cast<void (*)(bw::BwdArgs, int)>(const_cast<void*>(pl.f));
+    e = launch_kernel(kernel, dim3(static_cast<unsigned>(pl.grid)), dim3(pl.threads), pl.smem,
+                      c.stream, c.pdl, p, pl.stages);
+  } else {
+    auto kernel = reinterpret_cast<void (*)(bw::BwdArgs)>(const_cast<void*>(pl.f));
+    e = launch_kernel(kernel, dim3(static_cast<unsigned>(pl.grid)), dim3(pl.threads), pl.smem,
+                      c.stream, c.pdl, p);
+  }
   if (e != cudaSuccess) {
     note_cuda_error(static_cast<int>(e));
     return ADDLN_ERR_LAUNCH;

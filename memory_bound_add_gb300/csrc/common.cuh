@@ -318,17 +318,23 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 // Waits for phase `parity` of the barrier, giving up after limit_ns
 // nanoseconds (limit 0: give up without waiting).  Returns true once the
-// phase has completed.
+// phase has completed.  try_wait gives up after a short, hardware-chosen
+// time, so a warp waiting on HBM would otherwise re-poll every ~100 ns and
+// take issue slots from the warps that are computing; between polls it
+// sleeps 64, 128, then 256 ns.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns) {
   constexpr uint32_t kSuspendNs = 20000;
   if (limit_ns == 0) return false;
   if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity, kSuspendNs)) {
+  uint32_t sleep_ns = 64;
+  for (;;) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
     if (global_timer_ns() - t0 > limit_ns) return false;
+    if (sleep_ns < 256) sleep_ns <<= 1;
   }
-  return true;
 }
 
 // ------------------------------------------------------------- statistics

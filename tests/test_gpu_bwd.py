@@ -85,6 +85,22 @@ def test_shapes(dtype, H):
     check(case, dtype, out, f"37x{H} {dtype} {p}")
 
 
+@pytest.mark.parametrize("stages", [1, 2, 3, 4])
+@pytest.mark.parametrize("name", ["tiny_64x768_fp32", "cancel_65536x1000_bf16",
+                                  "pages_2048x4096_fp16", "large_32768x8192_bf16"])
+def test_ring_depths(name, stages):
+    # the staging ring's depth changes only the launch, never the grid (so the
+    # workspace size is the same for every depth)
+    w = synth.with_rows(synth.get(name), 150)
+    case = make_case(w, seed=5)
+    prev = mba.addln_set_cta_shape(0, stages)
+    try:
+        out, p = run(case)
+    finally:
+        mba.addln_set_cta_shape(prev, 0)
+    check(case, w.dtype, out, f"{name} ring {stages} {p}")
+
+
 def test_deterministic_and_in_place():
     w = synth.with_rows(synth.get("large_32768x8192_bf16"), 300)
     case = make_case(w, seed=3)
