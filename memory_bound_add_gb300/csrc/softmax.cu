@@ -237,16 +237,65 @@ __global__ void __launch_bounds__(THREADS) k_softmax_cta(const RowArgs p) {
 }
 
 // ------------------------------------------- CTA per row, long rows (TMA)
+// Largest value of a 16-byte vector (the non-NaN operand of a pair, as
+// fmaxf); 16-bit vectors are compared as packed pairs, without widening.
+template <int DT>
+__device__ __forceinline__ float vec_max(const uint4& u) {
+  if constexpr (DT == kF32) {
+    return fmaxf(fmaxf(__uint_as_float(u.x), __uint_as_float(u.y)),
+                 fmaxf(__uint_as_float(u.z), __uint_as_float(u.w)));
+  } else if constexpr (DT == kF16) {
+    const __half2 a = __hmax2(*reinterpret_cast<const __half2*>(&u.x), *reinterpret_cast<const __half2*>(&u.y));
+    const __half2 b = __hmax2(*reinterpret_cast<const __half2*>(&u.z), *reinterpret_cast<const __half2*>(&u.w));
+    const __half2 c = __hmax2(a, b);
+    return __half2float(__hmax(__low2half(c), __high2half(c)));
+  } else {
+    const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u.x),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u.z),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&u.w));
+    const __nv_bfloat162 c = __hmax2(a, b);
+    return __bfloat162float(__hmax(__low2bfloat16(c), __high2bfloat16(c)));
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// exp(d) = 2^(d log2 e), by the hardware base-2 exponential (PTX
+// ex2.approx, relative error about 2^-22), on a pair of values.  Results
+// below 2^-126 flush to zero (.ftz): far under the 1e-12 absolute floor of
+// any softmax output that matters, and one instruction instead of several.
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float ex2(float t) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+  return r;
+}
+__device__ __forceinline__ float2 exp_pair(float2 v, float2 negm, float2 log2e) {
+  const float2 t = mul2(add2(v, negm), log2e);
+  return make_float2(ex2(t.x), ex2(t.y));
+}
+
 // Rows too long to sit in the registers of several CTAs per SM (more than
-// 2048 16-byte vectors) stay in their staged shared-memory copy and are read
-// twice: pass 1 keeps a running (max, sum of exp) per thread, rescaling the
-// sum when the maximum grows; pass 2 writes exp(x - M) / S.  Two exponentials
-// per element, but a quarter of the registers, so three CTAs (rows) per SM
-// stream instead of one.
+// 2048 16-byte vectors) stay in their staged shared-memory copy (three CTAs,
+// rows, per SM) and are read three times: the row maximum M (16-bit values
+// compared as packed pairs), then S = sum exp(x - M), then y = exp(x - M) / S
+// (fp32 pair arithmetic).  With M known before any exponential is taken the
+// sum needs no rescaling, and the passes issue about a third of the
+// instructions of a running (max, sum) pass.  Warp w owns the contiguous
+// chunk w of every row (ceil(vectors / warps) vectors), staged by its own
+// bulk copy onto its own mbarrier: it starts as soon as its chunk lands, and
+// once it has written its chunk of y it refills the chunk with the CTA's next
+// row while the other warps are still normalising theirs.
 template <int DT, int THREADS>
 __global__ void __launch_bounds__(THREADS) k_softmax_cta_smem(const RowArgs p) {
   using IO = Io<DT>;
   constexpr int VEC = IO::kVec;
+  constexpr int P = VEC / 2;
   constexpr int S = IO::kBytes;
   constexpr int NW = THREADS / 32;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -254,13 +303,21 @@ __global__ void __launch_bounds__(THREADS) k_softmax_cta_smem(const RowArgs p) {
   const int nvec = p.H / VEC;
   const uint32_t row_bytes = static_cast<uint32_t>(p.H) * S;  // multiple of 16
   const uint32_t rb = (row_bytes + 127u) & ~127u;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + rb);
-  SPart* red = reinterpret_cast<SPart*>(smem + rb + 16);  // [2][NW]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + rb);  // [NW]
+  float* redm = reinterpret_cast<float*>(smem + rb + 8u * NW);  // [NW] warp maxima
+  float* reds = redm + NW;                                       // [NW] warp sums
   const uint32_t xs = smem_addr(smem);
-  const uint32_t bar_a = smem_addr(bar);
+  const uint32_t bar_w = smem_addr(&bars[warp]);
+  // this warp's chunk of every row: vectors [c0, c0 + cvecs)
+  const int cw = (nvec + NW - 1) / NW;
+  const int c0 = min(warp * cw, nvec);
+  const int cvecs = min(cw, nvec - c0);
+  const uint32_t chunk_off = static_cast<uint32_t>(c0) * 16u;
+  const uint32_t chunk_bytes = static_cast<uint32_t>(cvecs) * 16u;
+  const float2 log2e = dup2(kLog2e);
 
   if (tid == 0) {
-    mbar_init(bar_a, 1);
+    for (int w = 0; w < NW; ++w) mbar_init(smem_addr(&bars[w]), 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -270,56 +327,65 @@ __global__ void __launch_bounds__(THREADS) k_softmax_cta_smem(const RowArgs p) {
 
   const int64_t stride = gridDim.x;
   int64_t row = blockIdx.x;
-  auto issue = [&](int64_t rr) {
-    mbar_arrive_expect_tx(bar_a, row_bytes);
-    bulk_g2s(xs, static_cast<const char*>(p.x) + rr * static_cast<int64_t>(row_bytes), row_bytes,
-             bar_a, policy);
+  auto issue = [&](int64_t rr) {  // lane 0: the warp's chunk of row rr
+    mbar_arrive_expect_tx(bar_w, chunk_bytes);
+    if (chunk_bytes != 0)
+      bulk_g2s(xs + chunk_off,
+               static_cast<const char*>(p.x) + rr * static_cast<int64_t>(row_bytes) + chunk_off,
+               chunk_bytes, bar_w, policy);
   };
-  if (tid == 0 && row < p.rows) issue(row);
+  if (lane == 0 && row < p.rows) issue(row);
 
   for (int64_t it = 0; row < p.rows; ++it, row += stride) {
-    const bool timed_out = !mbar_wait_bounded(bar_a, static_cast<uint32_t>(it & 1), p.wait_limit_ns);
-    // pass 1: running max and rescaled exp-sum over this thread's vectors
-    SPart mine{-INFINITY, 0.f};
-    for (int c = tid; c < nvec; c += THREADS) {
-      float v[VEC];
-      IO::unpack(ld_shared_v4(xs + c * 16), v);
-      float m8 = v[0];
+    const bool timed_out =
+        __any_sync(0xffffffffu, !mbar_wait_bounded(bar_w, static_cast<uint32_t>(it & 1), p.wait_limit_ns));
+    // pass 1: the row maximum
+    float mx = -INFINITY;
+    if (!timed_out)
+      for (int c = c0 + lane; c < c0 + cvecs; c += 32) mx = fmaxf(mx, vec_max<DT>(ld_shared_v4(xs + c * 16)));
 #pragma unroll
-      for (int e = 1; e < VEC; ++e) m8 = fmaxf(m8, v[e]);
-      const float mn = fmaxf(mine.m, m8);
-      const float mb = mn == -INFINITY ? 0.f : mn;
-      float s8 = 0.f;
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) s8 += __expf(v[e] - mb);
-      mine.s = mine.s * rescale(mine.m, mn) + s8;
-      mine.m = mn;
-    }
-    const SPart wp = butterfly<32>(mine);
-    SPart* rbuf = red + (it & 1) * NW;
-    if (lane == 0) rbuf[warp] = wp;
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) redm[warp] = mx;
     if (__syncthreads_or(timed_out)) {
       if (tid == 0) {
+        // each warp's chunk of this row is the only copy in flight
         atomicExch(&g_softmax_error, ADDLN_ERR_DEVICE_TIMEOUT);
-        mbar_wait_bounded(bar_a, static_cast<uint32_t>(it & 1), 1000000000ull);
+        for (int w = 0; w < NW; ++w)
+          mbar_wait_bounded(smem_addr(&bars[w]), static_cast<uint32_t>(it & 1), 1000000000ull);
       }
       return;
     }
-    const SPart tot = butterfly<NW>(rbuf[lane % NW]);
-    const float mb = tot.m == -INFINITY ? 0.f : tot.m;
-    const float inv = 1.0f / tot.s;
-    // pass 2: normalise from the staged copy
-    char* yrow = static_cast<char*>(p.y) + row * static_cast<int64_t>(row_bytes);
-    for (int c = tid; c < nvec; c += THREADS) {
-      float v[VEC];
-      IO::unpack(ld_shared_v4(xs + c * 16), v);
+    mx = redm[lane % NW];
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) v[e] = __expf(v[e] - mb) * inv;
-      st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::pack(v));
+    for (int off = 1; off < NW; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float2 negm = dup2(mx == -INFINITY ? 0.f : -mx);
+    // pass 2: S = sum exp(x - M)
+    float2 acc = dup2(0.f);
+    for (int c = c0 + lane; c < c0 + cvecs; c += 32) {
+      float2 v[P];
+      IO::to_pairs(ld_shared_v4(xs + c * 16), v);
+#pragma unroll
+      for (int q = 0; q < P; ++q) acc = add2(acc, exp_pair(v[q], negm, log2e));
     }
-    // every thread is done with the staged row before it is refilled
+    float sum = warp_sum(acc.x + acc.y);
+    if (lane == 0) reds[warp] = sum;
     __syncthreads();
-    if (tid == 0 && row + stride < p.rows) issue(row + stride);
+    sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) sum += reds[w];
+    const float2 inv = dup2(1.0f / sum);
+    // pass 3: normalise this warp's chunk from the staged copy
+    char* yrow = static_cast<char*>(p.y) + row * static_cast<int64_t>(row_bytes);
+    for (int c = c0 + lane; c < c0 + cvecs; c += 32) {
+      float2 v[P];
+      IO::to_pairs(ld_shared_v4(xs + c * 16), v);
+#pragma unroll
+      for (int q = 0; q < P; ++q) v[q] = mul2(exp_pair(v[q], negm, log2e), inv);
+      st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::from_pairs(v));
+    }
+    // every lane of the warp is done with its chunk before it is refilled
+    __syncwarp();
+    if (lane == 0 && row + stride < p.rows) issue(row + stride);
   }
 }
 
@@ -472,7 +538,7 @@ template <int DT>
 int smem_launch(const RowArgs& p, const LaunchCtx& c) {
   constexpr int THREADS = 256;
   const uint32_t row_bytes = static_cast<uint32_t>(p.H) * Io<DT>::kBytes;
-  const uint32_t smem = ((row_bytes + 127u) & ~127u) + 16u + 2u * (THREADS / 32) * sizeof(SPart);
+  const uint32_t smem = ((row_bytes + 127u) & ~127u) + 16u * (THREADS / 32);
   if (smem > static_cast<uint32_t>(c.dev.smem_optin)) return ADDLN_ERR_UNSUPPORTED;
   const void* f = reinterpret_cast<const void*>(&k_softmax_cta_smem<DT, THREADS>);
   const int per_sm = resident(f, THREADS, static_cast<int>(smem), c.dev);
