@@ -511,11 +511,11 @@ __global__ void __launch_bounds__(THREADS) k_bwd_scalar(const BwdArgs p) {
 // dgamma_j = sum_b ws[b][0][j], dbeta_j = sum_b ws[b][1][j].  A block covers
 // 32 columns with 16 slices of the partials (slice s takes b = s, s + 16,
 // ...; a warp reads 32 adjacent columns of one partial, 128 coalesced
-// bytes); each thread keeps four accumulators over interleaved subsequences
-// of its slice, so four loads are in flight, then adds them in a fixed
+// bytes); each thread keeps eight accumulators over interleaved subsequences
+// of its slice, so eight loads are in flight, then adds them in a fixed
 // order; the 16 slice sums are added in slice order.  The result does not
 // depend on scheduling.
-constexpr int kColCols = 32, kColSlices = 16, kColAcc = 4;
+constexpr int kColCols = 32, kColSlices = 16, kColAcc = 8;
 
 __global__ void __launch_bounds__(kColCols * kColSlices, 2) k_colsum(const float* ws, int64_t G, int H,
                                                                      float* dgamma, float* dbeta) {
@@ -525,7 +525,9 @@ __global__ void __launch_bounds__(kColCols * kColSlices, 2) k_colsum(const float
   const int lc = threadIdx.x % kColCols, sl = threadIdx.x / kColCols;
   const int j = blockIdx.x * kColCols + lc;
   const int64_t ld = 2 * static_cast<int64_t>(H);
-  float acc[kColAcc] = {0.f, 0.f, 0.f, 0.f};
+  float acc[kColAcc];
+#pragma unroll
+  for (int u = 0; u < kColAcc; ++u) acc[u] = 0.f;
   if (j < 2 * H) {
     constexpr int64_t kStep = static_cast<int64_t>(kColSlices) * kColAcc;
     for (int64_t b = sl; b < G; b += kStep) {
@@ -536,7 +538,7 @@ __global__ void __launch_bounds__(kColCols * kColSlices, 2) k_colsum(const float
       }
     }
   }
-  part[sl][lc] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  part[sl][lc] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
   __syncthreads();
   if (sl == 0 && j < 2 * H) {
     float t = part[0][lc];
