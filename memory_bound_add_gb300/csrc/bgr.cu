@@ -39,8 +39,45 @@ __device__ __forceinline__ float gelu(float v) {
   return 0.5f * v * (v >= 0.f ? 2.0f - erfc_a : erfc_a);
 }
 
+// The same GELU on a pair of values, in fp32 pair arithmetic: every step but
+// the reciprocal, the exponential and the sign select covers both values in
+// one instruction.  exp(-a^2) = 2^(-a^2 log2 e) by the hardware base-2
+// exponential (PTX ex2.approx.ftz: results below 2^-126 flush to zero,
+// where the GELU term is far below any output's rounding).
+__device__ __forceinline__ float ex2_ftz(float t) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+  return r;
+}
+
+__device__ __forceinline__ float2 gelu2(float2 v) {
+  constexpr float p = 0.3275911f;
+  constexpr float a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f,
+                  a4 = -1.453152027f, a5 = 1.061405429f;
+  constexpr float kNegLog2e = -1.4426950408889634f;
+  const float2 a = mul2(make_float2(fabsf(v.x), fabsf(v.y)), dup2(0.70710678118654752f));
+  const float2 den = fma2(dup2(p), a, dup2(1.0f));
+  const float2 t = make_float2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y));
+  float2 q = fma2(t, dup2(a5), dup2(a4));
+  q = fma2(t, q, dup2(a3));
+  q = fma2(t, q, dup2(a2));
+  q = fma2(t, q, dup2(a1));
+  const float2 arg = mul2(mul2(a, a), dup2(kNegLog2e));
+  const float2 erfc_a = mul2(mul2(t, q), make_float2(ex2_ftz(arg.x), ex2_ftz(arg.y)));
+  const float2 two_minus = add2(dup2(2.0f), make_float2(-erfc_a.x, -erfc_a.y));
+  const float2 w = make_float2(v.x >= 0.f ? two_minus.x : erfc_a.x, v.y >= 0.f ? two_minus.y : erfc_a.y);
+  return mul2(mul2(dup2(0.5f), v), w);
+}
+
 // What each element becomes.  kBgr: GELU(x + b) + r; kBias: x + b; kGelu: GELU(x).
 enum Kind { kBgr = 0, kBias = 1, kGelu = 2 };
+
+template <int KIND>
+__device__ __forceinline__ float2 apply2(float2 x, float2 r, float2 b) {
+  if constexpr (KIND == kBgr) return add2(gelu2(add2(x, b)), r);
+  if constexpr (KIND == kBias) return add2(x, b);
+  return gelu2(x);
+}
 
 template <int KIND>
 __device__ __forceinline__ float apply(float x, float r, float b) {
@@ -95,21 +132,23 @@ __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* 
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t i = i0 + static_cast<int64_t>(u) * kThreads;
       if (i < nvec) {
-        float f[VEC], g[VEC], b[VEC];
-        IO::unpack(xs[u], f);
-        if constexpr (HAS_R) IO::unpack(rs[u], g);
+        constexpr int P = VEC / 2;
+        float2 f[P], g[P], b[P];
+        IO::to_pairs(xs[u], f);
+        if constexpr (HAS_R) IO::to_pairs(rs[u], g);
         if constexpr (HAS_B) {
           const float* bp = bias + cols[u] * VEC;
 #pragma unroll
           for (int q = 0; q < VEC / 4; ++q) {
             const float4 t = ld_param_f4(bp + 4 * q);
-            b[4 * q] = t.x; b[4 * q + 1] = t.y; b[4 * q + 2] = t.z; b[4 * q + 3] = t.w;
+            b[2 * q] = make_float2(t.x, t.y);
+            b[2 * q + 1] = make_float2(t.z, t.w);
           }
         }
 #pragma unroll
-        for (int e = 0; e < VEC; ++e)
-          f[e] = apply<KIND>(f[e], HAS_R ? g[e] : 0.f, HAS_B ? b[e] : 0.f);
-        st_stream_v4(yv + i, IO::pack(f));
+        for (int q = 0; q < P; ++q)
+          f[q] = apply2<KIND>(f[q], HAS_R ? g[q] : dup2(0.f), HAS_B ? b[q] : dup2(0.f));
+        st_stream_v4(yv + i, IO::from_pairs(f));
       }
     }
   }
