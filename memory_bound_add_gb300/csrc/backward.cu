@@ -315,17 +315,17 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
     // The CTA form keeps dY (packed) and xhat in registers across the row
     // sums; the warp form, holding twice the columns, reads both again from
     // its slot, which it refills only after the row is done.
+    // (timed_out is warp-uniform: the whole block is skipped, not selected
+    // element by element; a slot that is not ok is never read)
     constexpr int KEEP = ROWWARP ? 1 : NV;
     uint4 dv[KEEP];
     float2 xh[KEEP][P];
     float2 sg2 = dup2(0.f), sgx2 = dup2(0.f);
+    if (!timed_out) {
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int kk = ROWWARP ? 0 : k;
-      dv[kk] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int q = 0; q < P; ++q) xh[kk][q] = dup2(0.f);
-      if (ok[k] && !timed_out) {
+      if (ok[k]) {
         dv[kk] = ld_shared_v4(region(s) + (32 * k + lane) * 16);
         IO::to_pairs(ld_shared_v4(region(s) + CV * 16u + (32 * k + lane) * 16), xh[kk]);
         float2 d[P];
@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
           }
         }
       }
+    }
     }
     float tg = warp_sum(sg2.x + sg2.y), tgx = warp_sum(sgx2.x + sgx2.y);
     if constexpr (ROWWARP) {
