@@ -77,7 +77,7 @@ def test_incoming_a_gradient(name):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
-@pytest.mark.parametrize("H", [1, 8, 33, 1000, 1024, 1025, 4096, 8192, 12288])
+@pytest.mark.parametrize("H", [1, 8, 33, 1000, 1024, 1025, 1032, 2056, 4096, 4104, 8192, 12288])
 def test_shapes(dtype, H):
     w = synth.custom(37, H, dtype, x_dist=(2.0, 1.5), want_resid=True, want_stats=True)
     case = make_case(w, seed=H)

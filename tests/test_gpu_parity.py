@@ -142,7 +142,7 @@ def test_output_combinations(name, want_a, want_stats):
 
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
 @pytest.mark.parametrize("H", [1, 2, 7, 8, 9, 31, 32, 33, 255, 257, 1000, 1001, 1023, 1024, 1025,
-                               2048, 4095, 4097, 8192, 12288])
+                               1032, 2048, 2056, 4095, 4097, 4104, 8192, 12288])
 @pytest.mark.parametrize("rows", [1, 3, 33])
 def test_shape_sweep(dtype, H, rows):
     w = synth.custom(rows, H, dtype, x_dist=(3.0, 2.0), want_resid=True, want_stats=True)
