@@ -510,17 +510,20 @@ __global__ void __launch_bounds__(THREADS) k_bwd_scalar(const BwdArgs p) {
 }
 
 // dgamma_j = sum_b ws[b][0][j], dbeta_j = sum_b ws[b][1][j].  A block covers
-// 32 columns with 16 slices of the partials (slice s takes b = s, s + 16,
-// ...; a warp reads 32 adjacent columns of one partial, 128 coalesced
-// bytes); each thread keeps eight accumulators over interleaved subsequences
-// of its slice, so eight loads are in flight, then adds them in a fixed
-// order; the 16 slice sums are added in slice order.  The result does not
-// depend on scheduling.
-constexpr int kColCols = 32, kColSlices = 16, kColAcc = 8;
+// 32 columns with SLICES slices of the partials (slice s takes b = s,
+// s + SLICES, ...; a warp reads 32 adjacent columns of one partial, 128
+// coalesced bytes); each thread keeps eight accumulators over interleaved
+// subsequences of its slice, so eight loads are in flight, then adds them in
+// a fixed order; the slice sums are added in slice order.  The result does
+// not depend on scheduling.  Narrow rows (few 32-column blocks) take 32
+// slices, so that each thread has fewer partials to walk.
+constexpr int kColCols = 32, kColAcc = 8;
 
-__global__ void __launch_bounds__(kColCols * kColSlices, 2) k_colsum(const float* ws, int64_t G, int H,
-                                                                     float* dgamma, float* dbeta) {
-  __shared__ float part[kColSlices][kColCols + 1];
+template <int SLICES>
+__global__ void __launch_bounds__(kColCols * SLICES, 32 / SLICES) k_colsum(const float* ws, int64_t G,
+                                                                            int H, float* dgamma,
+                                                                            float* dbeta) {
+  __shared__ float part[SLICES][kColCols + 1];
   pdl_trigger();
   pdl_wait();
   const int lc = threadIdx.x % kColCols, sl = threadIdx.x / kColCols;
@@ -530,11 +533,11 @@ __global__ void __launch_bounds__(kColCols * kColSlices, 2) k_colsum(const float
 #pragma unroll
   for (int u = 0; u < kColAcc; ++u) acc[u] = 0.f;
   if (j < 2 * H) {
-    constexpr int64_t kStep = static_cast<int64_t>(kColSlices) * kColAcc;
+    constexpr int64_t kStep = static_cast<int64_t>(SLICES) * kColAcc;
     for (int64_t b = sl; b < G; b += kStep) {
 #pragma unroll
       for (int u = 0; u < kColAcc; ++u) {
-        const int64_t bu = b + static_cast<int64_t>(u) * kColSlices;
+        const int64_t bu = b + static_cast<int64_t>(u) * SLICES;
         if (bu < G) acc[u] += ws[bu * ld + j];
       }
     }
@@ -544,7 +547,7 @@ __global__ void __launch_bounds__(kColCols * kColSlices, 2) k_colsum(const float
   if (sl == 0 && j < 2 * H) {
     float t = part[0][lc];
 #pragma unroll 8
-    for (int q = 1; q < kColSlices; ++q) t += part[q][lc];
+    for (int q = 1; q < SLICES; ++q) t += part[q][lc];
     if (j < H)
       dgamma[j] = t;
     else
@@ -599,15 +602,11 @@ struct Plan {
   const char* name = "none";
 };
 
-// One wave of resident CTAs, but no more than needed to give every CTA about
-// four rows (fewer partials to write and sum) and never fewer than two per SM.
+// One wave of resident CTAs (no more than there are rows for).
 int64_t grid_of(int64_t rows, int64_t per_cta_rows, int per_sm, const DeviceInfo& dev) {
-  int64_t wave = static_cast<int64_t>(per_sm) * dev.sms;
-  int64_t want = (rows + 4 * per_cta_rows - 1) / (4 * per_cta_rows);
-  if (want < 2 * static_cast<int64_t>(dev.sms)) want = 2 * static_cast<int64_t>(dev.sms);
-  int64_t g = want < wave ? want : wave;
+  const int64_t wave = static_cast<int64_t>(per_sm) * dev.sms;
   const int64_t need = (rows + per_cta_rows - 1) / per_cta_rows;
-  if (g > need) g = need;
+  const int64_t g = need < wave ? need : wave;
   return g < 1 ? 1 : g;
 }
 
@@ -771,10 +770,15 @@ int launch_bwd(int dtype, const void* dy, const void* a, const float* mean, cons
   }
   if (want_cols) {
     const int64_t cols = 2 * H;
-    e = launch_kernel(bw::k_colsum, dim3(static_cast<unsigned>((cols + bw::kColCols - 1) / bw::kColCols)),
-                      dim3(bw::kColCols * bw::kColSlices), 0,
-                      c.stream, c.pdl, static_cast<const float*>(ws), partials,
-                      static_cast<int>(H), dgamma, dbeta);
+    const int64_t blocks = (cols + bw::kColCols - 1) / bw::kColCols;
+    if (blocks < c.dev.sms)
+      e = launch_kernel(bw::k_colsum<32>, dim3(static_cast<unsigned>(blocks)), dim3(bw::kColCols * 32),
+                        0, c.stream, c.pdl, static_cast<const float*>(ws), partials,
+                        static_cast<int>(H), dgamma, dbeta);
+    else
+      e = launch_kernel(bw::k_colsum<16>, dim3(static_cast<unsigned>(blocks)), dim3(bw::kColCols * 16),
+                        0, c.stream, c.pdl, static_cast<const float*>(ws), partials,
+                        static_cast<int>(H), dgamma, dbeta);
     if (e != cudaSuccess) {
       note_cuda_error(static_cast<int>(e));
       return ADDLN_ERR_LAUNCH;
