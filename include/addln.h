@@ -92,6 +92,45 @@ int add_layernorm_fwd(const void *x, const void *r, const float *gamma, const fl
                       int64_t rows, int64_t H, float eps, int dtype, void *stream);
 
 /*
+ * add_layernorm_fwd from HOST buffers to HOST buffers, the host-device
+ * copies inside the call (the pages' operation, end to end; the pages have
+ * no host-side entry point of their own).
+ *   x_host, r_host        [rows, H] inputs in dtype, host memory (required)
+ *   gamma_host, beta_host [H] fp32, host memory (required)
+ *   y_host                [rows, H] output in dtype, host memory (required)
+ *   resid_out_host        [rows, H] A = X + R rounded to dtype, or NULL
+ *   mean_host, rstd_host  [rows] fp32, each independently NULL-able
+ *   workspace             device memory of at least
+ *                         add_layernorm_fwd_host_workspace_size(rows, H,
+ *                         dtype, resid_out_host != NULL, mean_host || rstd_host)
+ *                         bytes, 256-byte aligned; owned by the caller, not
+ *                         touched by any other call while this one runs
+ *   stream                the caller's stream; the kernels run on it, and it
+ *                         waits for the last copy back, so synchronising it
+ *                         completes the call
+ * Rows go through in chunks of about 4 MiB of X, pipelined over a copy-in
+ * stream, `stream` and a copy-out stream (created once per device on the
+ * first call, which should come before any stream capture), so both copy
+ * directions and the kernels overlap; each copy is one cudaMemcpyAsync.
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to run asynchronously; pageable memory is correct but slower.
+ * y_host and resid_out_host may equal x_host or r_host exactly (in place);
+ * any other overlap is ADDLN_ERR_ALIAS.  Results are those of
+ * add_layernorm_fwd on the same rows.  Errors as add_layernorm_fwd, plus
+ * ADDLN_ERR_WORKSPACE.  Calls on one device are serialised while they queue
+ * their work; they are safe from several host threads.
+ */
+int add_layernorm_fwd_host(const void *x_host, const void *r_host, const float *gamma_host,
+                           const float *beta_host, void *y_host, void *resid_out_host,
+                           float *mean_host, float *rstd_host, int64_t rows, int64_t H, float eps,
+                           int dtype, void *workspace, int64_t workspace_bytes, void *stream);
+
+/* Device workspace bytes add_layernorm_fwd_host needs (0 for rows == 0), or
+ * a negative code for an invalid shape or dtype. */
+int64_t add_layernorm_fwd_host_workspace_size(int64_t rows, int64_t H, int dtype, int want_resid,
+                                              int want_stats);
+
+/*
  * Unfused baseline, step 1: A = X + R rounded to dtype, elementwise over n
  * contiguous elements ("算子融合的收益量化" section 1, the separate Residual
  * Add kernel: two reads, one write).  a may equal x or r exactly.

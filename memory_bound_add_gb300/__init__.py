@@ -6,6 +6,8 @@ the C ABI of ``include/addln.h``); ``binding`` marshals PyTorch tensors to it.
 from .binding import (  # noqa: F401
     AddLNError,
     add_layernorm_fwd,
+    add_layernorm_fwd_host,
+    add_layernorm_fwd_host_workspace_size,
     add_fwd,
     layernorm_fwd,
     add_layernorm,

@@ -33,6 +33,10 @@ _I64 = ctypes.c_int64
 SIGNATURES = {
     "add_layernorm_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
                                          ctypes.c_float, ctypes.c_int, _P]),
+    "add_layernorm_fwd_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                                              ctypes.c_float, ctypes.c_int, _P, _I64, _P]),
+    "add_layernorm_fwd_host_workspace_size": (ctypes.c_int64, [_I64, _I64, ctypes.c_int,
+                                                               ctypes.c_int, ctypes.c_int]),
     "add_fwd": (ctypes.c_int, [_P, _P, _P, _I64, ctypes.c_int, _P]),
     "layernorm_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_float,
                                      ctypes.c_int, _P]),
@@ -167,6 +171,65 @@ def add_layernorm_fwd(x, r, gamma, beta, y, resid_out=None, mean=None, rstd=None
                                  _ptr(resid_out), _ptr(mean), _ptr(rstd), int(rows), int(H),
                                  float(eps), int(dtype), _stream(stream))
     _check(rc, "add_layernorm_fwd")
+
+
+def _require_host(t, name, dtype=None, like=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if like is not None and t.numel() != like.numel():
+        raise ValueError(f"{name} has {t.numel()} elements, expected {like.numel()}")
+
+
+def add_layernorm_fwd_host_workspace_size(rows: int, H: int, dtype: int, want_resid: bool = False,
+                                          want_stats: bool = False) -> int:
+    n = int(lib().add_layernorm_fwd_host_workspace_size(int(rows), int(H), int(dtype),
+                                                         int(bool(want_resid)), int(bool(want_stats))))
+    if n < 0:
+        raise AddLNError(n, "add_layernorm_fwd_host_workspace_size")
+    return n
+
+
+def add_layernorm_fwd_host(x, r, gamma, beta, y, resid_out=None, mean=None, rstd=None,
+                           eps: float = 1e-5, workspace=None, stream=None):
+    """add_layernorm_fwd from host tensors to host tensors (pinned for overlap).
+
+    The copies to and from the GPU happen inside the call; `workspace` is a
+    CUDA uint8 tensor of at least add_layernorm_fwd_host_workspace_size(...)
+    bytes (allocated here when omitted).  Synchronise `stream` (default: the
+    current stream) before reading the outputs.
+    """
+    rows, H = _rows_shape(x)
+    dtype = DTYPE_CODE.get(x.dtype)
+    if dtype is None:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    for t, n in ((x, "x"), (r, "r"), (y, "y"), (resid_out, "resid_out")):
+        if t is not None:
+            _require_host(t, n, x.dtype, like=x)
+    for t, n in ((gamma, "gamma"), (beta, "beta")):
+        _require_host(t, n, torch.float32)
+        if t.numel() != H:
+            raise ValueError(f"{n} must have H={H} elements")
+    for t, n in ((mean, "mean"), (rstd, "rstd")):
+        if t is not None:
+            _require_host(t, n, torch.float32)
+            if t.numel() != rows:
+                raise ValueError(f"{n} must have rows={rows} elements")
+    need = add_layernorm_fwd_host_workspace_size(rows, H, dtype, resid_out is not None,
+                                                 mean is not None or rstd is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    rc = lib().add_layernorm_fwd_host(_ptr(x), _ptr(r), _ptr(gamma), _ptr(beta), _ptr(y),
+                                      _ptr(resid_out), _ptr(mean), _ptr(rstd), int(rows), int(H),
+                                      float(eps), int(dtype), _ptr(workspace),
+                                      int(workspace.numel() * workspace.element_size()),
+                                      _stream(stream))
+    _check(rc, "add_layernorm_fwd_host")
 
 
 def layernorm_fwd(a, gamma, beta, y, mean=None, rstd=None, eps: float = 1e-5, stream=None,

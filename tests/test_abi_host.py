@@ -43,7 +43,8 @@ def header_defines():
 
 def test_header_declares_the_expected_entry_points():
     assert header_functions() == sorted([
-        "add_layernorm_fwd", "add_fwd", "layernorm_fwd", "softmax_fwd", "bias_gelu_residual_fwd",
+        "add_layernorm_fwd", "add_layernorm_fwd_host", "add_layernorm_fwd_host_workspace_size",
+        "add_fwd", "layernorm_fwd", "softmax_fwd", "bias_gelu_residual_fwd",
         "bias_add_fwd", "gelu_fwd", "add_layernorm_bwd", "add_layernorm_bwd_workspace_size",
         "add_layernorm_bwd_noalloc",
         "addln_strerror",
@@ -135,6 +136,43 @@ def test_validation_codes(lib):
     # rows == 0 is a no-op once dtype, H and eps are valid, even with NULLs
     assert fused(lib, rows=0, x=None, y=None) == b.OK
     assert fused(lib, rows=0, dtype=9) == b.ERR_DTYPE
+
+
+def host_fused(lib, x=BASE, r=BASE + 0x1000000, g=BASE + 0x2000000, bt=BASE + 0x2100000,
+               y=BASE + 0x3000000, a=None, mean=None, rstd=None, rows=4, H=8, eps=1e-5, dtype=0,
+               ws=BASE + 0x4000000, ws_bytes=1 << 20):
+    return lib.add_layernorm_fwd_host(x, r, g, bt, y, a, mean, rstd, rows, H, eps, dtype, ws,
+                                      ws_bytes, None)
+
+
+def test_host_entry_validation_before_any_cuda_call(lib):
+    # every rejection below is decided on the host, before the first CUDA call
+    from memory_bound_add_gb300 import binding as b
+    assert host_fused(lib, dtype=3) == b.ERR_DTYPE
+    assert host_fused(lib, H=0) == b.ERR_SHAPE
+    assert host_fused(lib, rows=-1) == b.ERR_SHAPE
+    assert host_fused(lib, eps=-1.0) == b.ERR_EPS
+    assert host_fused(lib, eps=float("nan")) == b.ERR_EPS
+    for k in ("x", "r", "g", "bt", "y"):
+        assert host_fused(lib, **{k: None}) == b.ERR_NULL
+    assert host_fused(lib, rows=0, x=None, y=None) == b.OK
+    need = lib.add_layernorm_fwd_host_workspace_size(4, 8, b.FP32, 0, 0)
+    assert need > 0
+    assert host_fused(lib, ws=None) == b.ERR_WORKSPACE
+    assert host_fused(lib, ws_bytes=need - 1) == b.ERR_WORKSPACE
+    assert host_fused(lib, ws=BASE + 0x4000010, ws_bytes=need) == b.ERR_WORKSPACE  # not 256-aligned
+    # y may be x exactly, not partly; a must lie apart from y
+    assert host_fused(lib, y=BASE + 64, ws_bytes=need) == b.ERR_ALIAS
+    assert host_fused(lib, a=BASE + 0x3000000, ws_bytes=need) == b.ERR_ALIAS
+    assert host_fused(lib, mean=BASE + 0x2000000 + 8, rstd=BASE + 0x5000000, ws_bytes=need) == b.ERR_ALIAS
+    # workspace sizes: outputs add buffers; chunks of about 4 MiB of X
+    assert lib.add_layernorm_fwd_host_workspace_size(0, 8, b.FP32, 0, 0) == 0
+    assert lib.add_layernorm_fwd_host_workspace_size(4, 8, 7, 0, 0) == b.ERR_DTYPE
+    base = lib.add_layernorm_fwd_host_workspace_size(2048, 4096, b.FP16, 0, 0)
+    assert lib.add_layernorm_fwd_host_workspace_size(2048, 4096, b.FP16, 1, 0) > base
+    assert lib.add_layernorm_fwd_host_workspace_size(2048, 4096, b.FP16, 0, 1) > base
+    # two 512-row chunk buffers of X, R, Y (4 MiB each) plus gamma and beta
+    assert base == 2 * 3 * 512 * 4096 * 2 + 2 * 4096 * 4
 
 
 def test_alias_rules(lib):

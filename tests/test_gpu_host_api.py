@@ -1,0 +1,98 @@
+"""add_layernorm_fwd_host (host buffers in and out, copies inside the call):
+the same results as add_layernorm_fwd on device buffers, bit for bit, over
+chunkings with a ragged last chunk, every output combination, pageable and
+page-locked memory and in-place use; and the oracle on one case."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+import synth
+from test_gpu_parity import check
+
+pytestmark = pytest.mark.gpu
+mba = pytest.importorskip("memory_bound_add_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from memory_bound_add_gb300.build import build
+    build()
+    yield
+
+
+def device_reference(d, want_a, want_stats):
+    x, r = d["x"].cuda(), d["r"].cuda()
+    g, b = d["gamma"].cuda(), d["beta"].cuda()
+    y = torch.empty_like(x)
+    a = torch.empty_like(x) if want_a else None
+    m = torch.empty(x.shape[0], device="cuda") if want_stats else None
+    s = torch.empty(x.shape[0], device="cuda") if want_stats else None
+    mba.add_layernorm_fwd(x, r, g, b, y, a, m, s, eps=d["eps"])
+    torch.cuda.synchronize()
+    return [t.cpu() if t is not None else None for t in (y, a, m, s)]
+
+
+def host_call(d, want_a, want_stats, pin=True, in_place=False):
+    prep = (lambda t: t.clone().pin_memory()) if pin else (lambda t: t.clone())
+    hx, hr, hg, hb = prep(d["x"]), prep(d["r"]), prep(d["gamma"]), prep(d["beta"])
+    hy = hx if in_place else prep(torch.empty_like(d["x"]))
+    ha = prep(torch.empty_like(d["x"])) if want_a else None
+    hm = prep(torch.empty(d["x"].shape[0])) if want_stats else None
+    hs = prep(torch.empty(d["x"].shape[0])) if want_stats else None
+    mba.add_layernorm_fwd_host(hx, hr, hg, hb, hy, ha, hm, hs, eps=d["eps"])
+    torch.cuda.synchronize()
+    return [hy, ha, hm, hs]
+
+
+CASES = [
+    ("pages_2048x4096_fp16", 2048),     # four 512-row chunks
+    ("pages_2048x4096_fp16", 1000),     # 512 + 488
+    ("cancel_65536x1000_bf16", 5000),   # 2097 + 2097 + 806
+    ("large_32768x8192_bf16", 300),     # 256 + 44
+    ("tiny_64x768_fp32", 64),           # one chunk
+    ("tail_4096x1001_bf16", 777),       # misaligned rows: element kernels on device
+]
+
+
+@pytest.mark.parametrize("name,rows", CASES)
+@pytest.mark.parametrize("want_a,want_stats", [(False, False), (True, True)])
+def test_matches_device_entry_point_bitwise(name, rows, want_a, want_stats):
+    w = synth.with_rows(synth.get(name), rows)
+    d = synth.make_inputs(w, seed=21)
+    ref = device_reference(d, want_a, want_stats)
+    got = host_call(d, want_a, want_stats)
+    for u, v in zip(got, ref):
+        assert (u is None) == (v is None)
+        if u is not None:
+            assert torch.equal(u, v)
+
+
+def test_pageable_memory_and_in_place():
+    w = synth.with_rows(synth.get("pages_2048x4096_fp16"), 1500)
+    d = synth.make_inputs(w, seed=22)
+    ref = device_reference(d, False, False)
+    assert torch.equal(host_call(d, False, False, pin=False)[0], ref[0])
+    assert torch.equal(host_call(d, False, False, in_place=True)[0], ref[0])
+
+
+def test_mean_without_rstd():
+    w = synth.with_rows(synth.get("cancel_65536x1000_bf16"), 3000)
+    d = synth.make_inputs(w, seed=23)
+    ref = device_reference(d, False, True)
+    hx, hr = d["x"].pin_memory(), d["r"].pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    hm = torch.empty(w.rows).pin_memory()
+    mba.add_layernorm_fwd_host(hx, hr, d["gamma"], d["beta"], hy, mean=hm, eps=d["eps"])
+    torch.cuda.synchronize()
+    assert torch.equal(hy, ref[0]) and torch.equal(hm, ref[2])
+
+
+def test_against_the_oracle():
+    w = synth.with_rows(synth.get("cancel_65536x1000_bf16"), 3000)
+    d = synth.make_inputs(w, seed=24)
+    hy, ha, hm, hs = host_call(d, True, True)
+    out = {"y": hy, "a": ha, "mean": hm, "rstd": hs, "path": "host"}
+    check(w, d, out, "host entry point")
