@@ -608,6 +608,55 @@ def oracle_rows_call(w, d, lo, hi):
                                        want_stats=w.want_stats)
 
 
+def _oracle_worker(job):
+    """One process of the row-parallel oracle leg: the oracle as it stands on
+    its own block of rows, repeated until `seconds` of work are done."""
+    op, dtype, eps, want_a, want_stats, x, r, gamma, beta, seconds = job
+    import oracle
+    def call():
+        if op == "softmax":
+            return oracle.oracle_softmax(x, dtype)
+        if op == "bias_gelu_residual":
+            return oracle.oracle_bias_gelu_residual(x, r, beta, dtype)
+        return oracle.oracle_add_layernorm(x, r, gamma, beta, eps, dtype, want_a=want_a,
+                                           want_stats=want_stats)
+    call()                                             # load outside the timing
+    done, t0 = 0, time.perf_counter()
+    while True:
+        call()
+        done += x.shape[0]
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done, el
+
+
+def cpu_baseline_parallel(w, d, seconds, cores):
+    """The same oracle in `cores` processes (spawned: no GPU state is
+    inherited), each on its own block of rows of the batch."""
+    import multiprocessing as mp
+    n_rows = max(1, min(w.rows // cores, (32 << 20) // max(1, 2 * w.H * w.elem_bytes)))
+    jobs = []
+    for k in range(cores):
+        lo = (k * n_rows) % max(1, w.rows - n_rows + 1)
+        x = d["x"][lo:lo + n_rows].clone()
+        r = d["r"][lo:lo + n_rows].clone() if w.op != "softmax" else None
+        jobs.append((w.op, w.dtype, d["eps"], w.want_resid, w.want_stats, x, r, d["gamma"],
+                     d["beta"], seconds))
+    from concurrent.futures import ProcessPoolExecutor
+    try:
+        with ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn")) as ex:
+            res = list(ex.map(_oracle_worker, jobs, timeout=seconds + 120))
+    except Exception as e:                 # a broken pool reports, never hangs
+        return {"error": f"row-parallel oracle leg failed: {type(e).__name__}"}
+    rows_done = sum(r[0] for r in res)
+    el = max(r[1] for r in res)
+    per_row = w.algorithmic_bytes() / w.rows
+    return {"value": round(rows_done * per_row / el / 1e9, 4), "unit": "GB/s",
+            "rows_per_s": round(rows_done / el, 1), "cores": cores,
+            "sample": f"{cores} processes, each {n_rows} rows of {w.name} repeated for "
+                      f"{seconds:.0f} s ({rows_done} rows in all), fp64 C oracle"}
+
+
 def cpu_baseline(w, d, seconds):
     """The fp64 oracle as it stands (single-threaded C), timed on whole
     batches of the workload until `seconds` of work have been done."""
@@ -623,11 +672,14 @@ def cpu_baseline(w, d, seconds):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": round(done_rows * per_row / el / 1e9, 4), "unit": "GB/s",
-            "rows_per_s": round(done_rows / el, 1), "cores": 1, "kind": "oracle",
-            "sample": f"{batches} whole batches of {w.name} ({done_rows} rows) in {el:.1f} s, "
-                      "single-threaded fp64 C oracle",
-            "host_cores_available": cpu_cores(), "cpu_model": cpu_model()}
+    out = {"value": round(done_rows * per_row / el / 1e9, 4), "unit": "GB/s",
+           "rows_per_s": round(done_rows / el, 1), "cores": 1, "kind": "oracle",
+           "sample": f"{batches} whole batches of {w.name} ({done_rows} rows) in {el:.1f} s, "
+                     "single-threaded fp64 C oracle",
+           "host_cores_available": cpu_cores(), "cpu_model": cpu_model()}
+    if cpu_cores() > 1:
+        out["row_parallel"] = cpu_baseline_parallel(w, d, seconds, cpu_cores())
+    return out
 
 
 def run_reference(args):
