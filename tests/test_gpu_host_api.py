@@ -96,3 +96,48 @@ def test_against_the_oracle():
     hy, ha, hm, hs = host_call(d, True, True)
     out = {"y": hy, "a": ha, "mean": hm, "rstd": hs, "path": "host"}
     check(w, d, out, "host entry point")
+
+
+def test_two_host_threads_at_once():
+    # the copy streams are shared per device: calls from two threads queue
+    # behind one another there, each on its own stream, with correct results
+    import threading
+    cases = []
+    for k, (name, rows) in enumerate([("pages_2048x4096_fp16", 1700), ("cancel_65536x1000_bf16", 6000)]):
+        w = synth.with_rows(synth.get(name), rows)
+        d = synth.make_inputs(w, seed=30 + k)
+        cases.append((d, device_reference(d, True, True)))
+    results = [None, None]
+    errors = []
+
+    def worker(i):
+        try:
+            d, _ = cases[i]
+            s = torch.cuda.Stream()
+            outs = []
+            for _ in range(3):
+                with torch.cuda.stream(s):
+                    hx, hr = d["x"].pin_memory(), d["r"].pin_memory()
+                    hy = torch.empty_like(hx).pin_memory()
+                    ha = torch.empty_like(hx).pin_memory()
+                    hm = torch.empty(hx.shape[0]).pin_memory()
+                    hs = torch.empty(hx.shape[0]).pin_memory()
+                    mba.add_layernorm_fwd_host(hx, hr, d["gamma"], d["beta"], hy, ha, hm, hs,
+                                               eps=d["eps"], stream=s)
+                    s.synchronize()
+                    outs.append((hy, ha, hm, hs))
+            results[i] = outs
+        except Exception as e:   # reported below
+            errors.append(e)
+
+    ts = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors
+    for i in range(2):
+        ref = cases[i][1]
+        for outs in results[i]:
+            for u, v in zip(outs, ref):
+                assert torch.equal(u, v)
