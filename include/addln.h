@@ -210,7 +210,9 @@ int add_layernorm_bwd(const void *dy, const void *a, const float *mean, const fl
                       void *stream);
 
 /* Bytes of workspace add_layernorm_bwd needs for rows x H in dtype on the
- * current device (0 when rows == 0), or a negative code. */
+ * current device (0 when rows == 0): the larger of what 16-byte-aligned and
+ * unaligned rows need, counting only the kinds of rows the library can run
+ * at this H.  A negative code on error. */
 int64_t add_layernorm_bwd_workspace_size(int64_t rows, int64_t H, int dtype);
 
 /* Size of the built-in scratch buffer add_layernorm_bwd_noalloc uses. */

@@ -317,11 +317,14 @@ int64_t add_layernorm_bwd_workspace_size(int64_t rows, int64_t H, int dtype) {
   DeviceInfo dev;
   const int rc = device_info(&dev);
   if (rc != ADDLN_OK) return rc;
-  // the larger of the vector and the element plan: the pointers decide later
+  // the larger of the vector and the element plan (the pointers decide
+  // later); a plan that cannot run these rows at all (the element path above
+  // its shared-memory limit) does not count
   const int64_t v = addln::bwd_workspace_bytes(dtype, rows, H, true, dev);
   const int64_t s = addln::bwd_workspace_bytes(dtype, rows, H, false, dev);
-  if (v < 0) return v;
-  if (s < 0) return s;
+  if (v < 0 && v != ADDLN_ERR_UNSUPPORTED) return v;
+  if (s < 0 && s != ADDLN_ERR_UNSUPPORTED) return s;
+  if (v < 0 && s < 0) return ADDLN_ERR_UNSUPPORTED;
   return v > s ? v : s;
 }
 
