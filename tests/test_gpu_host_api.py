@@ -141,3 +141,28 @@ def test_two_host_threads_at_once():
         for outs in results[i]:
             for u, v in zip(outs, ref):
                 assert torch.equal(u, v)
+
+
+def _host_draw(n, seed):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        dtype = ["fp32", "fp16", "bf16"][rng.integers(3)]
+        H = int(rng.choice([7, 64, 768, 1000, 1001, 2048, 4096, 5000, 8192]))
+        rows = int(rng.integers(1, 3000))
+        flags = int(rng.integers(4))
+        out.append((rows, H, dtype, bool(flags & 1), bool(flags & 2)))
+    return out
+
+
+@pytest.mark.parametrize("rows,H,dtype,want_a,want_stats", _host_draw(12, 2030))
+def test_random_shapes_match_device_entry_point(rows, H, dtype, want_a, want_stats):
+    w = synth.custom(rows, H, dtype, x_dist=(1.0, 2.0))
+    d = synth.make_inputs(w, seed=rows + H)
+    ref = device_reference(d, want_a, want_stats)
+    got = host_call(d, want_a, want_stats)
+    for u, v in zip(got, ref):
+        assert (u is None) == (v is None)
+        if u is not None:
+            assert torch.equal(u, v)
