@@ -3,16 +3,20 @@
 // (max reduce, exp-sum reduce, divide), with the three passes fused into one
 // read of the row and one write.
 //
-// Each thread keeps its slice of the row in fp32 registers, takes its own
-// maximum m_t and replaces every value by e_j = exp(x_j - m_t) (one
-// exponential per element), summing s_t = sum e_j.  Partials (m, s) merge
-// with the online-softmax update
-//     m = max(m_a, m_b),  s = s_a * exp(m_a - m) + s_b * exp(m_b - m),
-// whose two terms are computed the same way on either side, so the xor
-// butterfly leaves identical totals (M, S) in every lane.  The output is
-// y_j = e_j * (exp(m_t - M) / S).  exp is CUDA's __expf (hardware base-2
-// exponential); its error grows with |x - max| but stays below 1e-5 relative
-// wherever the result is above 1e-30.
+// Two ways to reach (M, S) = (max, sum exp(x - M)):
+// - max first (warp-per-row vector kernel, long-row kernel): reduce M, then
+//   S = sum exp(x_j - M) and y_j = exp(x_j - M) / S, in fp32 pairs with
+//   exp(d) = 2^(d log2 e) on the hardware base-2 exponential (relative error
+//   about 2^-22; results under 2^-126 flush to zero).
+// - one pass (register-held CTA kernel, element kernels): each thread takes
+//   its own maximum m_t, replaces every value by e_j = exp(x_j - m_t) and sums
+//   s_t = sum e_j; partials (m, s) merge with the online-softmax update
+//       m = max(m_a, m_b),  s = s_a * exp(m_a - m) + s_b * exp(m_b - m),
+//   whose two terms are computed the same way on either side, so the xor
+//   butterfly leaves identical totals (M, S) in every lane, and
+//   y_j = e_j * (exp(m_t - M) / S).  exp here is CUDA's __expf; its error
+//   grows with |x - max| but stays below 1e-5 relative wherever the result
+//   is above 1e-30.
 //
 // Kernels: one warp per row for H <= 1024 (16-byte vector or element loads);
 // one CTA per row for longer rows, the row staged into shared memory by a TMA
@@ -96,10 +100,59 @@ __device__ __forceinline__ SPart thread_part(float (&v)[NV][VEC], const bool (&o
   return SPart{mx, s};
 }
 
+// Largest value of a 16-byte vector (the non-NaN operand of a pair, as
+// fmaxf); 16-bit vectors are compared as packed pairs, without widening.
+template <int DT>
+__device__ __forceinline__ float vec_max(const uint4& u) {
+  if constexpr (DT == kF32) {
+    return fmaxf(fmaxf(__uint_as_float(u.x), __uint_as_float(u.y)),
+                 fmaxf(__uint_as_float(u.z), __uint_as_float(u.w)));
+  } else if constexpr (DT == kF16) {
+    const __half2 a = __hmax2(*reinterpret_cast<const __half2*>(&u.x), *reinterpret_cast<const __half2*>(&u.y));
+    const __half2 b = __hmax2(*reinterpret_cast<const __half2*>(&u.z), *reinterpret_cast<const __half2*>(&u.w));
+    const __half2 c = __hmax2(a, b);
+    return __half2float(__hmax(__low2half(c), __high2half(c)));
+  } else {
+    const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u.x),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u.z),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&u.w));
+    const __nv_bfloat162 c = __hmax2(a, b);
+    return __bfloat162float(__hmax(__low2bfloat16(c), __high2bfloat16(c)));
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// exp(d) = 2^(d log2 e), by the hardware base-2 exponential (PTX
+// ex2.approx, relative error about 2^-22), on a pair of values.  Results
+// below 2^-126 flush to zero (.ftz): far under the 1e-12 absolute floor of
+// any softmax output that matters, and one instruction instead of several.
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float ex2(float t) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+  return r;
+}
+__device__ __forceinline__ float2 exp_pair(float2 v, float2 negm, float2 log2e) {
+  const float2 t = mul2(add2(v, negm), log2e);
+  return make_float2(ex2(t.x), ex2(t.y));
+}
+
 // ------------------------------------------------------ warp per row
 constexpr int kWarpCtaThreads = 256;
 constexpr int kRowsPerCta = kWarpCtaThreads / 32;
 
+// 16-byte rows: the warp's maximum M first (16-bit values compared as packed
+// pairs, then a five-step xor butterfly), so every exponential is
+// exp(x - M) and the sum needs no rescaling; exponentials, their sum and
+// the scaling by 1/S run on fp32 pairs.  Element rows: each thread keeps
+// exp(x - m_t) of its own elements and the (m, s) partials merge by the
+// online update.
 template <int DT, int NV, bool VECTOR, bool FULL>
 __global__ void __launch_bounds__(kWarpCtaThreads, 2) k_softmax_warp(const RowArgs p) {
   using IO = Io<DT>;
@@ -116,43 +169,53 @@ __global__ void __launch_bounds__(kWarpCtaThreads, 2) k_softmax_warp(const RowAr
   bool ok[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k) ok[k] = FULL || (lane + 32 * k) < nvec;
-  float v[NV][VEC];
-#pragma unroll
-  for (int k = 0; k < NV; ++k)
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
 
   if constexpr (VECTOR) {
+    constexpr int P = VEC / 2;
     const char* xrow = static_cast<const char*>(p.x) + base * S;
     uint4 xv[NV];
 #pragma unroll
     for (int k = 0; k < NV; ++k)
       if (ok[k]) xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(lane + 32 * k) * 16);
+    float mx = -INFINITY;
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (ok[k]) IO::unpack(xv[k], v[k]);
-  } else {
+      if (ok[k]) mx = fmaxf(mx, vec_max<DT>(xv[k]));
 #pragma unroll
-    for (int k = 0; k < NV; ++k)
-      if (ok[k]) v[k][0] = IO::load1(p.x, base + lane + 32 * k);
-  }
-
-  const SPart mine = thread_part<NV, VEC, FULL>(v, ok);
-  const SPart tot = butterfly<32>(mine);
-  const float f = rescale(mine.m, tot.m) / tot.s;
-
-  if constexpr (VECTOR) {
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    // a row that is all -inf gives exp(-inf) = 0 terms, not exp(NaN)
+    const float2 negm = dup2(mx == -INFINITY ? 0.f : -mx);
+    const float2 log2e = dup2(kLog2e);
+    float2 e[NV][P];
+    float2 acc[2] = {dup2(0.f), dup2(0.f)};
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (ok[k]) {
+        IO::to_pairs(xv[k], e[k]);
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          e[k][q] = exp_pair(e[k][q], negm, log2e);
+          acc[q & 1] = add2(acc[q & 1], e[k][q]);
+        }
+      }
+    }
+    const float2 inv = dup2(1.0f / warp_sum((acc[0].x + acc[1].x) + (acc[0].y + acc[1].y)));
     char* yrow = static_cast<char*>(p.y) + base * S;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       if (ok[k]) {
-        float o[VEC];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) o[e] = v[k][e] * f;
-        st_stream_v4(yrow + static_cast<int64_t>(lane + 32 * k) * 16, IO::pack(o));
+        for (int q = 0; q < P; ++q) e[k][q] = mul2(e[k][q], inv);
+        st_stream_v4(yrow + static_cast<int64_t>(lane + 32 * k) * 16, IO::from_pairs(e[k]));
       }
     }
   } else {
+    float v[NV][1];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) v[k][0] = ok[k] ? IO::load1(p.x, base + lane + 32 * k) : 0.f;
+    const SPart mine = thread_part<NV, 1, FULL>(v, ok);
+    const SPart tot = butterfly<32>(mine);
+    const float f = rescale(mine.m, tot.m) / tot.s;
 #pragma unroll
     for (int k = 0; k < NV; ++k)
       if (ok[k]) IO::store1(p.y, base + lane + 32 * k, v[k][0] * f);
@@ -237,49 +300,6 @@ __global__ void __launch_bounds__(THREADS) k_softmax_cta(const RowArgs p) {
 }
 
 // ------------------------------------------- CTA per row, long rows (TMA)
-// Largest value of a 16-byte vector (the non-NaN operand of a pair, as
-// fmaxf); 16-bit vectors are compared as packed pairs, without widening.
-template <int DT>
-__device__ __forceinline__ float vec_max(const uint4& u) {
-  if constexpr (DT == kF32) {
-    return fmaxf(fmaxf(__uint_as_float(u.x), __uint_as_float(u.y)),
-                 fmaxf(__uint_as_float(u.z), __uint_as_float(u.w)));
-  } else if constexpr (DT == kF16) {
-    const __half2 a = __hmax2(*reinterpret_cast<const __half2*>(&u.x), *reinterpret_cast<const __half2*>(&u.y));
-    const __half2 b = __hmax2(*reinterpret_cast<const __half2*>(&u.z), *reinterpret_cast<const __half2*>(&u.w));
-    const __half2 c = __hmax2(a, b);
-    return __half2float(__hmax(__low2half(c), __high2half(c)));
-  } else {
-    const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u.x),
-                                     *reinterpret_cast<const __nv_bfloat162*>(&u.y));
-    const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u.z),
-                                     *reinterpret_cast<const __nv_bfloat162*>(&u.w));
-    const __nv_bfloat162 c = __hmax2(a, b);
-    return __bfloat162float(__hmax(__low2bfloat16(c), __high2bfloat16(c)));
-  }
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
-
-// exp(d) = 2^(d log2 e), by the hardware base-2 exponential (PTX
-// ex2.approx, relative error about 2^-22), on a pair of values.  Results
-// below 2^-126 flush to zero (.ftz): far under the 1e-12 absolute floor of
-// any softmax output that matters, and one instruction instead of several.
-constexpr float kLog2e = 1.4426950408889634f;
-__device__ __forceinline__ float ex2(float t) {
-  float r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
-  return r;
-}
-__device__ __forceinline__ float2 exp_pair(float2 v, float2 negm, float2 log2e) {
-  const float2 t = mul2(add2(v, negm), log2e);
-  return make_float2(ex2(t.x), ex2(t.y));
-}
-
 // Rows too long to sit in the registers of several CTAs per SM (more than
 // 2048 16-byte vectors) stay in their staged shared-memory copy (three CTAs,
 // rows, per SM) and are read three times: the row maximum M (16-bit values
