@@ -126,11 +126,16 @@ __global__ void __launch_bounds__(THREADS) k_bwd_cta(const BwdArgs p) {
     bulk_g2s(s0 + rb, static_cast<const char*>(p.a) + off, row_bytes, bar_a, policy);
   };
   if (tid == 0 && row < p.rows) issue(row);
+  // mean and rstd of the next row are loaded one row ahead, off the row's
+  // critical path
+  float mu_n = 0.f, rs_n = 0.f;
+  if (row < p.rows) mu_n = __ldg(p.mean + row), rs_n = __ldg(p.rstd + row);
 
   for (int64_t it = 0; row < p.rows; ++it, row += stride) {
     const int64_t boff = row * static_cast<int64_t>(row_bytes);
+    const float mu = mu_n, rs = rs_n;
+    if (row + stride < p.rows) mu_n = __ldg(p.mean + row + stride), rs_n = __ldg(p.rstd + row + stride);
     const bool timed_out = !mbar_wait_bounded(bar_a, static_cast<uint32_t>(it & 1), p.wait_limit_ns);
-    const float mu = __ldg(p.mean + row), rs = __ldg(p.rstd + row);
     uint4 dv[NV];       // dY kept packed; the stage is refilled after the barrier
     float xh[NV][VEC];
     float sg = 0.f, sgx = 0.f;
@@ -303,14 +308,20 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
     for (int q = 0; q < P; ++q) dg[k][q] = db[k][q] = dup2(0.f);
   }
 
+  // mean and rstd of the next row are loaded one row ahead, off the row's
+  // critical path
+  float mu_n = 0.f, rs_n = 0.f;
+  if (row < p.rows) mu_n = __ldg(p.mean + row), rs_n = __ldg(p.rstd + row);
+
   bool failed = false;
   for (int64_t it = 0; row < p.rows; ++it, row += stride) {
     const int s = static_cast<int>(it % stages);
+    const float mu = mu_n, rs = rs_n;
+    if (row + stride < p.rows) mu_n = __ldg(p.mean + row + stride), rs_n = __ldg(p.rstd + row + stride);
     // warp-uniform: every lane polls the warp's barrier with its own clock
     const bool timed_out = __any_sync(
         0xffffffffu, !mbar_wait_bounded(smem_addr(&bars[s * NW + warp]),
                                         static_cast<uint32_t>((it / stages) & 1), p.wait_limit_ns));
-    const float mu = __ldg(p.mean + row), rs = __ldg(p.rstd + row);
     const float2 negmu = dup2(-mu), rs2 = dup2(rs);
     // The CTA form keeps dY (packed) and xhat in registers across the row
     // sums; the warp form, holding twice the columns, reads both again from
