@@ -61,16 +61,14 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // After a wait of warp w ran out: waits (bounded) for that warp's copies
-// still in flight -- rows it .. it+stages-1 of its ring -- so that none lands
-// in shared memory the next CTA on this SM may reuse.
-__device__ __noinline__ void drain_res(uint64_t* bars, int stages, int nw, int w, int64_t it,
+// still in flight -- the row at ring position `ring` and the stages-1 rows
+// after it -- so that none lands in shared memory the next CTA on this SM may
+// reuse.
+__device__ __noinline__ void drain_res(uint64_t* bars, int stages, int nw, int w, uint32_t ring,
                                        int64_t row, int64_t stride, int64_t rows) {
-  for (int j = 0; j < stages; ++j) {
-    const int64_t itj = it + j;
+  for (int j = 0; j < stages; ++j, ring = ring_next(ring, stages))
     if (row + j * stride < rows)
-      mbar_wait_bounded(smem_addr(&bars[(itj % stages) * nw + w]),
-                        static_cast<uint32_t>((itj / stages) & 1), 1000000000ull);
-  }
+      mbar_wait_bounded(smem_addr(&bars[ring_slot(ring) * nw + w]), ring_phase(ring), 1000000000ull);
 }
 
 // ---------------------------------------------------- CTA per row (TMA)
@@ -255,9 +253,9 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
   const int nvec = H / VEC;
   const bool cols = p.ws != nullptr;
   const uint32_t row_bytes = static_cast<uint32_t>(H) * S;
-  const uint32_t ring = static_cast<uint32_t>(stages) * NW * kRegion;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring);  // [stages][NW]
-  float2* red = reinterpret_cast<float2*>(smem + ring + 8u * kMaxStagesRes * NW);  // [2][NW]
+  const uint32_t ring_bytes = static_cast<uint32_t>(stages) * NW * kRegion;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_bytes);  // [stages][NW]
+  float2* red = reinterpret_cast<float2*>(smem + ring_bytes + 8u * kMaxStagesRes * NW);  // [2][NW]
   const uint32_t smem0 = smem_addr(smem);
 
   const int v0 = ROWWARP ? lane : warp * CV + lane;
@@ -314,14 +312,15 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
   if (row < p.rows) mu_n = __ldg(p.mean + row), rs_n = __ldg(p.rstd + row);
 
   bool failed = false;
-  for (int64_t it = 0; row < p.rows; ++it, row += stride) {
-    const int s = static_cast<int>(it % stages);
+  uint32_t ring = 0;  // ring position of the row: slot, phase, parity
+  for (; row < p.rows; row += stride, ring = ring_next(ring, stages)) {
+    const int s = static_cast<int>(ring_slot(ring));
     const float mu = mu_n, rs = rs_n;
     if (row + stride < p.rows) mu_n = __ldg(p.mean + row + stride), rs_n = __ldg(p.rstd + row + stride);
     // warp-uniform: every lane polls the warp's barrier with its own clock
     const bool timed_out = __any_sync(
         0xffffffffu, !mbar_wait_bounded(smem_addr(&bars[s * NW + warp]),
-                                        static_cast<uint32_t>((it / stages) & 1), p.wait_limit_ns));
+                                        ring_phase(ring), p.wait_limit_ns));
     const float2 negmu = dup2(-mu), rs2 = dup2(rs);
     // The CTA form keeps dY (packed) and xhat in registers across the row
     // sums; the warp form, holding twice the columns, reads both again from
@@ -358,16 +357,16 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
     float tg = warp_sum(sg2.x + sg2.y), tgx = warp_sum(sgx2.x + sgx2.y);
     if constexpr (ROWWARP) {
       if (timed_out) {
-        if (lane == 0) drain_res(bars, stages, NW, warp, it, row, stride, p.rows);
+        if (lane == 0) drain_res(bars, stages, NW, warp, ring, row, stride, p.rows);
         failed = true;
         break;
       }
     } else {
-      float2* rbuf = red + (it & 1) * NW;
+      float2* rbuf = red + ring_parity(ring) * NW;
       if (lane == 0) rbuf[warp] = make_float2(tg, tgx);
       if (__syncthreads_or(timed_out)) {
         if (tid == 0)
-          for (int w = 0; w < NW; ++w) drain_res(bars, stages, NW, w, it, row, stride, p.rows);
+          for (int w = 0; w < NW; ++w) drain_res(bars, stages, NW, w, ring, row, stride, p.rows);
         failed = true;
         break;
       }

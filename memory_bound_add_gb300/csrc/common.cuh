@@ -316,6 +316,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// A ring of `stages` staging slots walked one row at a time, held in one
+// register: bit 0 the row's parity (alternates every row), bit 1 the slot's
+// mbarrier phase, bits 2 and up the slot.  For the it-th row: slot
+// it % stages, phase (it / stages) & 1, parity it & 1, advanced without a
+// division.
+__device__ __forceinline__ uint32_t ring_slot(uint32_t r) { return r >> 2; }
+__device__ __forceinline__ uint32_t ring_phase(uint32_t r) { return (r >> 1) & 1u; }
+__device__ __forceinline__ uint32_t ring_parity(uint32_t r) { return r & 1u; }
+__device__ __forceinline__ uint32_t ring_next(uint32_t r, int stages) {
+  const uint32_t par = (r & 1u) ^ 1u;
+  const uint32_t slot = (r >> 2) + 1u;
+  return slot == static_cast<uint32_t>(stages) ? ((((r >> 1) & 1u) ^ 1u) << 1) | par
+                                               : (slot << 2) | (r & 2u) | par;
+}
+
 // Waits for phase `parity` of the barrier, giving up after limit_ns
 // nanoseconds (limit 0: give up without waiting).  Returns true once the
 // phase has completed.  try_wait gives up after a short, hardware-chosen

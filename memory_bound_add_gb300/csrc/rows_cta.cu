@@ -48,18 +48,16 @@ __device__ __forceinline__ Part cta_totals(const Part* red, int lane) {
 }
 
 // After a wait ran out: flags the device error and waits (bounded) for the
-// copies still in flight -- every warp's chunk of rows it .. it+stages-1 of
-// the ring -- so that no copy lands in shared memory the next CTA on this SM
-// may reuse.
-__device__ __noinline__ void drain_after_timeout(uint64_t* bars, int stages, int nw, int64_t it,
+// copies still in flight -- every warp's chunk of the row at ring position
+// `ring` and of the stages-1 rows after it -- so that no copy lands in shared
+// memory the next CTA on this SM may reuse.
+__device__ __noinline__ void drain_after_timeout(uint64_t* bars, int stages, int nw, uint32_t ring,
                                                  int64_t row, int64_t stride, int64_t rows) {
   atomicExch(&g_device_error, ADDLN_ERR_DEVICE_TIMEOUT);
-  for (int j = 0; j < stages; ++j) {
-    const int64_t itj = it + j;
+  for (int j = 0; j < stages; ++j, ring = ring_next(ring, stages)) {
     if (row + j * stride >= rows) continue;
     for (int w = 0; w < nw; ++w)
-      mbar_wait_bounded(smem_addr(&bars[(itj % stages) * nw + w]),
-                        static_cast<uint32_t>((itj / stages) & 1), kDrainLimitNs);
+      mbar_wait_bounded(smem_addr(&bars[ring_slot(ring) * nw + w]), ring_phase(ring), kDrainLimitNs);
   }
 }
 
@@ -185,7 +183,9 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
     }
   }
 
-  for (int64_t it = 0; row < p.rows; ++it, row += stride) {
+  uint32_t ring = 0;  // ring position of the row: slot, phase, parity
+  for (; row < p.rows; row += stride, ring = ring_next(ring, stages)) {
+    const int s = static_cast<int>(ring_slot(ring));
     const int64_t base = row * static_cast<int64_t>(H);
     // the row's sums a = x + r as fp32 pairs, each thread's slice in registers
     float2 v[NV][P];
@@ -195,11 +195,10 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
       for (int q = 0; q < P; ++q) v[k][q] = dup2(0.f);
 
     bool timed_out = false;
-    const int s = TMA ? static_cast<int>(it % stages) : 0;
     if constexpr (TMA) {
       // the whole warp waits for its own chunk (one instruction a poll)
       timed_out = !mbar_wait_bounded(smem_addr(&bars[s * NW + warp]),
-                                     static_cast<uint32_t>((it / stages) & 1), p.wait_limit_ns);
+                                     ring_phase(ring), p.wait_limit_ns);
       if (!timed_out) {
         const uint32_t xs = smem0 + s * slot;
         if (has_r) {
@@ -255,14 +254,14 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
       for (int q = 0; q < P; ++q) v[k][q] = add2(v[k][q], negK);
     Part st = thread_part2<NV, P, FULL, false>(v, ok, negK);
     st = butterfly<FULL, 32>(st);
-    WarpPart* rbuf = red + (it & 1) * NW;
+    WarpPart* rbuf = red + ring_parity(ring) * NW;
     if (lane == 0) rbuf[warp] = WarpPart{Kw, st.n, st.m, st.M2};
 
     // ---- all warps' partials in; also the point after which no thread
     // reads slot s any more
     if constexpr (TMA) {
       if (__syncthreads_or(timed_out)) {
-        if (tid == 0) drain_after_timeout(bars, stages, NW, it, row, stride, p.rows);
+        if (tid == 0) drain_after_timeout(bars, stages, NW, ring, row, stride, p.rows);
         return;
       }
       if (lane == 0) {
