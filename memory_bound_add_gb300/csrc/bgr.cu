@@ -163,11 +163,19 @@ __global__ void __launch_bounds__(kThreads) k_ew_scalar(const void* x, const voi
   pdl_trigger();
   pdl_wait();
   const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads;
-  for (int64_t k = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; k < n; k += step) {
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  // the bias column k % H, carried along (step % H < H, so one wrap at most)
+  const int64_t smod = KIND != kGelu ? step % H : 0;
+  int64_t col = KIND != kGelu ? first % H : 0;
+  for (int64_t k = first; k < n; k += step) {
     const float xv = IO::load1(x, k);
     const float rv = KIND == kBgr ? IO::load1(r, k) : 0.f;
-    const float bv = KIND != kGelu ? __ldg(bias + k % H) : 0.f;
+    const float bv = KIND != kGelu ? __ldg(bias + col) : 0.f;
     IO::store1(y, k, apply<KIND>(xv, rv, bv));
+    if (KIND != kGelu) {
+      col += smod;
+      if (col >= H) col -= H;
+    }
   }
 }
 
