@@ -60,6 +60,14 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Two warp sums at once, added as a pair at every step.
+__device__ __forceinline__ float2 warp_sum2(float2 v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    v = add2(v, make_float2(__shfl_xor_sync(0xffffffffu, v.x, off), __shfl_xor_sync(0xffffffffu, v.y, off)));
+  return v;
+}
+
 // After a wait of warp w ran out: waits (bounded) for that warp's copies
 // still in flight -- the row at ring position `ring` and the stages-1 rows
 // after it -- so that none lands in shared memory the next CTA on this SM may
@@ -322,13 +330,17 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
         0xffffffffu, !mbar_wait_bounded(smem_addr(&bars[s * NW + warp]),
                                         ring_phase(ring), p.wait_limit_ns));
     const float2 negmu = dup2(-mu), rs2 = dup2(rs);
-    // The CTA form keeps dY (packed) and xhat in registers across the row
-    // sums; the warp form, holding twice the columns, reads both again from
-    // its slot, which it refills only after the row is done.
+    // The CTA form keeps xhat and either g = dY gamma (up to 256 threads) or
+    // dY still packed (512 threads, where holding g measured slower) in
+    // registers across the row sums; the warp form, holding twice the
+    // columns, reads dY and A again from its slot, which it refills only
+    // after the row is done.
     // (timed_out is warp-uniform: the whole block is skipped, not selected
     // element by element; a slot that is not ok is never read)
     constexpr int KEEP = ROWWARP ? 1 : NV;
-    uint4 dv[KEEP];
+    constexpr bool KEEPG = !ROWWARP && THREADS <= 256;
+    float2 gk[KEEPG ? KEEP : 1][P];
+    uint4 dv[KEEPG ? 1 : KEEP];
     float2 xh[KEEP][P];
     float2 sg2 = dup2(0.f), sgx2 = dup2(0.f);
     if (!timed_out) {
@@ -336,14 +348,16 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
     for (int k = 0; k < NV; ++k) {
       const int kk = ROWWARP ? 0 : k;
       if (ok[k]) {
-        dv[kk] = ld_shared_v4(region(s) + (32 * k + lane) * 16);
+        const uint4 dpk = ld_shared_v4(region(s) + (32 * k + lane) * 16);
+        if constexpr (!KEEPG) dv[kk] = dpk;
         IO::to_pairs(ld_shared_v4(region(s) + CV * 16u + (32 * k + lane) * 16), xh[kk]);
         float2 d[P];
-        IO::to_pairs(dv[kk], d);
+        IO::to_pairs(dpk, d);
 #pragma unroll
         for (int q = 0; q < P; ++q) {
           xh[kk][q] = mul2(add2(xh[kk][q], negmu), rs2);
           const float2 g = mul2(d[q], gam[k][q]);
+          if constexpr (KEEPG) gk[kk][q] = g;
           sg2 = add2(sg2, g);
           sgx2 = fma2(g, xh[kk][q], sgx2);
           if (cols) {
@@ -354,7 +368,8 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
       }
     }
     }
-    float tg = warp_sum(sg2.x + sg2.y), tgx = warp_sum(sgx2.x + sgx2.y);
+    const float2 ts = warp_sum2(make_float2(sg2.x + sg2.y, sgx2.x + sgx2.y));
+    float tg = ts.x, tgx = ts.y;
     if constexpr (ROWWARP) {
       if (timed_out) {
         if (lane == 0) drain_res(bars, stages, NW, warp, ring, row, stride, p.rows);
@@ -371,13 +386,21 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
         break;
       }
       if (lane == 0 && row + stages * stride < p.rows) issue(s, row + stages * stride);
-      tg = 0.f;
-      tgx = 0.f;
+      // the warps' (sum g, sum g xhat) pairs, two to a 16-byte load, added
+      // as pairs in a fixed tree
+      float2 t[NW];
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        tg += rbuf[w].x;
-        tgx += rbuf[w].y;
+      for (int w = 0; w < NW; w += 2) {
+        const float4 u = *reinterpret_cast<const float4*>(rbuf + w);
+        t[w] = make_float2(u.x, u.y);
+        t[w + 1] = make_float2(u.z, u.w);
       }
+#pragma unroll
+      for (int h = NW / 2; h > 0; h >>= 1)
+#pragma unroll
+        for (int w = 0; w < h; ++w) t[w] = add2(t[w], t[w + h]);
+      tg = t[0].x;
+      tgx = t[0].y;
     }
     // dA = rstd * (g - (xhat * mean(g xhat) + mean(g))) (+ dA_in)
     const float2 nmgx = dup2(-(tgx * p.inv_h)), nmg = dup2(-(tg * p.inv_h));
@@ -386,16 +409,30 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
     for (int k = 0; k < NV; ++k) {
       if (ok[k]) {
         const int c = v0 + 32 * k;
-        float2 d[P], o[P], rr[P], x[P];
+        float2 g[P], o[P], rr[P], x[P];
         if constexpr (ROWWARP) {
+          float2 d[P];
           IO::to_pairs(ld_shared_v4(region(s) + (32 * k + lane) * 16), d);
           IO::to_pairs(ld_shared_v4(region(s) + CV * 16u + (32 * k + lane) * 16), x);
 #pragma unroll
-          for (int q = 0; q < P; ++q) x[q] = mul2(add2(x[q], negmu), rs2);
+          for (int q = 0; q < P; ++q) {
+            x[q] = mul2(add2(x[q], negmu), rs2);
+            g[q] = mul2(d[q], gam[k][q]);
+          }
+        } else if constexpr (KEEPG) {
+#pragma unroll
+          for (int q = 0; q < P; ++q) {
+            x[q] = xh[k][q];
+            g[q] = gk[k][q];
+          }
         } else {
+          float2 d[P];
           IO::to_pairs(dv[k], d);
 #pragma unroll
-          for (int q = 0; q < P; ++q) x[q] = xh[k][q];
+          for (int q = 0; q < P; ++q) {
+            x[q] = xh[k][q];
+            g[q] = mul2(d[q], gam[k][q]);
+          }
         }
         if (p.dres != nullptr)
           IO::to_pairs(ld_stream_v4(static_cast<const char*>(p.dres) +
@@ -403,7 +440,7 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
                        rr);
 #pragma unroll
         for (int q = 0; q < P; ++q) {
-          o[q] = mul2(rs2, add2(mul2(d[q], gam[k][q]), fma2(x[q], nmgx, nmg)));
+          o[q] = mul2(rs2, add2(g[q], fma2(x[q], nmgx, nmg)));
           if (p.dres != nullptr) o[q] = add2(o[q], rr[q]);
         }
         st_stream_v4(drow + static_cast<int64_t>(c) * 16, IO::from_pairs(o));
