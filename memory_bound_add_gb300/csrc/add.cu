@@ -1,17 +1,17 @@
 // Unfused baseline, step 1: the separate residual-add kernel of
 // "算子融合的收益量化" section 1 -- read X and R, write A = X + R in the I/O
 // dtype (rounded to nearest-even from the fp32 sum).  Grid-stride over
-// 16-byte vectors with four independent vectors per thread per step; the
-// last n % VEC elements (and misaligned buffers) take element accesses.
+// 16-byte vectors with four independent vectors per thread per step (one on
+// short tensors, so that the whole grid has work); the last
+// n % VEC elements (and misaligned buffers) take element accesses.
 #include "../../include/addln.h"
 #include "common.cuh"
 
 namespace addln {
 
 constexpr int kAddThreads = 256;
-constexpr int kAddUnroll = 4;
 
-template <int DT>
+template <int DT, int UNROLL>
 __global__ void __launch_bounds__(kAddThreads) k_add_vec(const void* x, const void* r, void* a,
                                                          int64_t nvec, int64_t n) {
   using IO = Io<DT>;
@@ -21,12 +21,12 @@ __global__ void __launch_bounds__(kAddThreads) k_add_vec(const void* x, const vo
   uint4* av = static_cast<uint4*>(a);
   pdl_trigger();
   pdl_wait();
-  const int64_t step = static_cast<int64_t>(gridDim.x) * kAddThreads * kAddUnroll;
-  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kAddThreads * kAddUnroll + threadIdx.x;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kAddThreads * UNROLL;
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kAddThreads * UNROLL + threadIdx.x;
        i0 < nvec; i0 += step) {
-    uint4 xs[kAddUnroll], rs[kAddUnroll];
+    uint4 xs[UNROLL], rs[UNROLL];
 #pragma unroll
-    for (int u = 0; u < kAddUnroll; ++u) {
+    for (int u = 0; u < UNROLL; ++u) {
       const int64_t i = i0 + static_cast<int64_t>(u) * kAddThreads;
       if (i < nvec) {
         xs[u] = ld_stream_v4(xv + i);
@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kAddThreads) k_add_vec(const void* x, const vo
       }
     }
 #pragma unroll
-    for (int u = 0; u < kAddUnroll; ++u) {
+    for (int u = 0; u < UNROLL; ++u) {
       const int64_t i = i0 + static_cast<int64_t>(u) * kAddThreads;
       if (i < nvec) {
         float f[VEC], g[VEC];
@@ -72,11 +72,19 @@ static int launch_add_t(const void* x, const void* r, void* a, int64_t n, const 
   cudaError_t e;
   if (al(x) && al(r) && al(a)) {
     const int64_t nvec = n / VEC;
-    int64_t blocks = (nvec + kAddThreads * kAddUnroll - 1) / (kAddThreads * kAddUnroll);
+    // vectors a thread keeps in flight: 4, or 1 when a full grid would give
+    // each thread at most 2 (then every resident thread has work); the
+    // GELU kernels' middle setting, 2, measured slower here
+    const int64_t resident = max_blocks * kAddThreads;
+    const int U = nvec <= 2 * resident ? 1 : 4;
+    int64_t blocks = (nvec + kAddThreads * U - 1) / (kAddThreads * U);
     if (blocks > max_blocks) blocks = max_blocks;
     if (blocks < 1) blocks = 1;
-    e = launch_kernel(k_add_vec<DT>, dim3(static_cast<unsigned>(blocks)), dim3(kAddThreads), 0,
-                      c.stream, c.pdl, x, r, a, nvec, n);
+    const dim3 grid(static_cast<unsigned>(blocks));
+    e = U == 1 ? launch_kernel(k_add_vec<DT, 1>, grid, dim3(kAddThreads), 0, c.stream, c.pdl, x, r, a,
+                               nvec, n)
+               : launch_kernel(k_add_vec<DT, 4>, grid, dim3(kAddThreads), 0, c.stream, c.pdl, x, r, a,
+                               nvec, n);
   } else {
     int64_t blocks = (n + kAddThreads - 1) / kAddThreads;
     if (blocks > max_blocks) blocks = max_blocks;

@@ -9,9 +9,10 @@
 // kernel with its own HBM round trip: T = X + bias and U = GELU(T) (the third
 // step, Y = U + R, is add_fwd).
 //
-// All kernels stream 16-byte vectors grid-stride with four independent
-// vectors in flight per thread; element accesses serve misaligned buffers
-// and rows that are not whole vectors.
+// All kernels stream 16-byte vectors grid-stride with up to four
+// independent vectors in flight per thread (fewer on short tensors, so that
+// the whole grid has work); element accesses serve misaligned buffers and
+// rows that are not whole vectors.
 #include "../../include/addln.h"
 #include "common.cuh"
 
@@ -19,7 +20,6 @@ namespace addln {
 namespace ew {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
 
 // GELU(v) = v/2 * (1 + erf(v / sqrt 2)).  erf from Abramowitz and Stegun,
 // Handbook of Mathematical Functions (1964), formula 7.1.26 (after Hastings):
@@ -88,7 +88,7 @@ __device__ __forceinline__ float apply(float x, float r, float b) {
 
 // Vector path: every buffer 16-byte aligned, H a multiple of the vector width
 // (so a vector never straddles two rows and its bias slice is aligned).
-template <int DT, int KIND>
+template <int DT, int KIND, int UNROLL>
 __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* r, const float* bias,
                                                      void* y, int64_t nvec, int64_t hvec) {
   using IO = Io<DT>;
@@ -100,18 +100,18 @@ __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* 
   uint4* yv = static_cast<uint4*>(y);
   pdl_trigger();
   pdl_wait();
-  const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads * kUnroll;
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * kThreads * kUnroll + threadIdx.x;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads * UNROLL;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kThreads * UNROLL + threadIdx.x;
   // bias column of vector i is i % hvec; advanced incrementally (one add and
   // at most one subtraction a vector) instead of a 64-bit remainder each time
   const int64_t tmod = kThreads % hvec, smod = step % hvec;
   int64_t col0 = HAS_B ? first % hvec : 0;
   for (int64_t i0 = first; i0 < nvec; i0 += step) {
-    int64_t cols[kUnroll];
+    int64_t cols[UNROLL];
     if constexpr (HAS_B) {
       int64_t cc = col0;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
+      for (int u = 0; u < UNROLL; ++u) {
         cols[u] = cc;
         cc += tmod;
         if (cc >= hvec) cc -= hvec;
@@ -119,9 +119,9 @@ __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* 
       col0 += smod;
       if (col0 >= hvec) col0 -= hvec;
     }
-    uint4 xs[kUnroll], rs[kUnroll];
+    uint4 xs[UNROLL], rs[UNROLL];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < UNROLL; ++u) {
       const int64_t i = i0 + static_cast<int64_t>(u) * kThreads;
       if (i < nvec) {
         xs[u] = ld_stream_v4(xv + i);
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* 
       }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < UNROLL; ++u) {
       const int64_t i = i0 + static_cast<int64_t>(u) * kThreads;
       if (i < nvec) {
         constexpr int P = VEC / 2;
@@ -189,11 +189,22 @@ int launch_t(const void* x, const void* r, const float* bias, void* y, int64_t r
   cudaError_t e;
   if (H % VEC == 0 && al(x) && al(r) && al(y) && al(bias)) {
     const int64_t nvec = n / VEC;
-    int64_t blocks = (nvec + kThreads * kUnroll - 1) / (kThreads * kUnroll);
+    // vectors a thread keeps in flight: 4 for long tensors; fewer when a
+    // full grid would give each thread only a few vectors, so that every
+    // resident thread has work and its loads, arithmetic and stores are not
+    // one serial chain (1 up to 2 vectors a resident thread, 2 up to 32)
+    const int64_t resident = max_blocks * kThreads;
+    const int U = nvec <= 2 * resident ? 1 : nvec <= 32 * resident ? 2 : 4;
+    int64_t blocks = (nvec + kThreads * U - 1) / (kThreads * U);
     if (blocks > max_blocks) blocks = max_blocks;
     if (blocks < 1) blocks = 1;
-    e = launch_kernel(k_ew_vec<DT, KIND>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
-                      c.stream, c.pdl, x, r, bias, y, nvec, H / VEC);
+    const dim3 grid(static_cast<unsigned>(blocks));
+    e = U == 1   ? launch_kernel(k_ew_vec<DT, KIND, 1>, grid, dim3(kThreads), 0, c.stream, c.pdl, x, r,
+                                 bias, y, nvec, H / VEC)
+        : U == 2 ? launch_kernel(k_ew_vec<DT, KIND, 2>, grid, dim3(kThreads), 0, c.stream, c.pdl, x, r,
+                                 bias, y, nvec, H / VEC)
+                 : launch_kernel(k_ew_vec<DT, KIND, 4>, grid, dim3(kThreads), 0, c.stream, c.pdl, x, r,
+                                 bias, y, nvec, H / VEC);
   } else {
     int64_t blocks = (n + kThreads - 1) / kThreads;
     if (blocks > max_blocks) blocks = max_blocks;
