@@ -14,7 +14,7 @@
 
 namespace addln {
 
-constexpr int kWarpCtaThreads = 256;  // 8 rows per CTA
+constexpr int kWarpCtaThreads = 128;  // 4 rows per CTA
 constexpr int kRowsPerCta = kWarpCtaThreads / 32;
 
 // Register cap a lane: 64 while it holds at most 24 values (four 256-thread

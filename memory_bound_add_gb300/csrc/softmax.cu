@@ -144,7 +144,7 @@ __device__ __forceinline__ float2 exp_pair(float2 v, float2 negm, float2 log2e) 
 }
 
 // ------------------------------------------------------ warp per row
-constexpr int kWarpCtaThreads = 256;
+constexpr int kWarpCtaThreads = 128;
 constexpr int kRowsPerCta = kWarpCtaThreads / 32;
 
 // 16-byte rows: the warp's maximum M first (16-bit values compared as packed
