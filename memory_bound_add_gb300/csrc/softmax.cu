@@ -4,13 +4,15 @@
 // read of the row and one write.
 //
 // Two ways to reach (M, S) = (max, sum exp(x - M)):
-// - max first (warp-per-row vector kernel, long-row kernel): reduce M, then
-//   S = sum exp(x_j - M) and y_j = exp(x_j - M) / S, in fp32 pairs with
-//   exp(d) = 2^(d log2 e) on the hardware base-2 exponential (relative error
-//   about 2^-22; results under 2^-126 flush to zero).
-// - one pass (register-held CTA kernel, element kernels): each thread takes
-//   its own maximum m_t, replaces every value by e_j = exp(x_j - m_t) and sums
-//   s_t = sum e_j; partials (m, s) merge with the online-softmax update
+// - max first (the 16-byte vector kernels: warp per row, CTA per row, long
+//   rows): reduce M, then S = sum exp(x_j - M) and y_j = exp(x_j - M) / S,
+//   in fp32 pairs with exp(d) = 2^(d log2 e) on the hardware base-2
+//   exponential (relative error about 2^-22; results under 2^-126 flush to
+//   zero).
+// - one pass (element kernels, for rows that are not 16-byte aligned): each
+//   thread takes its own maximum m_t, replaces every value by
+//   e_j = exp(x_j - m_t) and sums s_t = sum e_j; partials (m, s) merge with
+//   the online-softmax update
 //       m = max(m_a, m_b),  s = s_a * exp(m_a - m) + s_b * exp(m_b - m),
 //   whose two terms are computed the same way on either side, so the xor
 //   butterfly leaves identical totals (M, S) in every lane, and
@@ -223,10 +225,18 @@ __global__ void __launch_bounds__(kWarpCtaThreads, 2) k_softmax_warp(const RowAr
 }
 
 // ------------------------------------------------------ CTA per row (TMA)
+// Max first, as in the warp kernel: the row's 16-byte vectors stay packed in
+// registers while the CTA agrees on the maximum M (warp maxima through
+// shared memory, one barrier, after which the staging slot is refilled);
+// then exp(x - M) on fp32 pairs and their sum S (warp sums, a second
+// barrier), and y = exp(x - M) / S.  Each buffer of the warps' partials
+// alternates with the row's parity, so a warp that runs ahead into the next
+// row never overwrites values a slower warp is still reading.
 template <int DT, int THREADS, int NV, bool FULL>
 __global__ void __launch_bounds__(THREADS) k_softmax_cta(const RowArgs p) {
   using IO = Io<DT>;
   constexpr int VEC = IO::kVec;
+  constexpr int P = VEC / 2;
   constexpr int S = IO::kBytes;
   constexpr int NW = THREADS / 32;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -235,9 +245,10 @@ __global__ void __launch_bounds__(THREADS) k_softmax_cta(const RowArgs p) {
   const uint32_t row_bytes = static_cast<uint32_t>(p.H) * S;  // multiple of 16
   const uint32_t rb = (row_bytes + 127u) & ~127u;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + rb);
-  SPart* red = reinterpret_cast<SPart*>(smem + rb + 16);  // [2][NW]
+  SPart* red = reinterpret_cast<SPart*>(smem + rb + 16);  // [2][NW]: warp maxima (m), sums (s)
   const uint32_t xs = smem_addr(smem);
   const uint32_t bar_a = smem_addr(bar);
+  const float2 log2e = dup2(kLog2e);
 
   bool ok[NV];
 #pragma unroll
@@ -261,39 +272,62 @@ __global__ void __launch_bounds__(THREADS) k_softmax_cta(const RowArgs p) {
   };
   if (tid == 0 && row < p.rows) issue(row);
 
-  for (int64_t it = 0; row < p.rows; ++it, row += stride) {
-    const int64_t base = row * static_cast<int64_t>(p.H);
-    const bool timed_out = !mbar_wait_bounded(bar_a, static_cast<uint32_t>(it & 1), p.wait_limit_ns);
-    float v[NV][VEC];
+  for (uint32_t par = 0; row < p.rows; par ^= 1u, row += stride) {
+    const bool timed_out = !mbar_wait_bounded(bar_a, par, p.wait_limit_ns);
+    uint4 raw[NV];
+    float mx = -INFINITY;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
-      if (ok[k]) IO::unpack(ld_shared_v4(xs + (tid + THREADS * k) * 16), v[k]);
+      if (ok[k] && !timed_out) {
+        raw[k] = ld_shared_v4(xs + (tid + THREADS * k) * 16);
+        mx = fmaxf(mx, vec_max<DT>(raw[k]));
+      }
     }
-    const SPart mine = thread_part<NV, VEC, FULL>(v, ok);
-    const SPart wp = butterfly<32>(mine);
-    SPart* rbuf = red + (it & 1) * NW;
-    if (lane == 0) rbuf[warp] = wp;
-    // every thread has its slice in registers: the stage may be refilled
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    SPart* rbuf = red + par * NW;
+    if (lane == 0) rbuf[warp].m = mx;
+    // every thread has its slice in registers: the slot may be refilled
     if (__syncthreads_or(timed_out)) {
       if (tid == 0) {
         atomicExch(&g_softmax_error, ADDLN_ERR_DEVICE_TIMEOUT);
-        mbar_wait_bounded(bar_a, static_cast<uint32_t>(it & 1), 1000000000ull);
+        mbar_wait_bounded(bar_a, par, 1000000000ull);
       }
       return;
     }
     if (tid == 0 && row + stride < p.rows) issue(row + stride);
-    const SPart tot = butterfly<NW>(rbuf[lane % NW]);
-    const float f = rescale(mine.m, tot.m) / tot.s;
-    char* yrow = static_cast<char*>(p.y) + base * S;
+    mx = rbuf[0].m;
+#pragma unroll
+    for (int w = 1; w < NW; ++w) mx = fmaxf(mx, rbuf[w].m);
+    // a row that is all -inf gives exp(-inf) = 0 terms, not exp(NaN)
+    const float2 negm = dup2(mx == -INFINITY ? 0.f : -mx);
+    float2 e[NV][P];
+    float2 acc[2] = {dup2(0.f), dup2(0.f)};
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       if (ok[k]) {
-        float o[VEC];
+        IO::to_pairs(raw[k], e[k]);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) o[e] = v[k][e] * f;
-        st_stream_v4(yrow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::pack(o));
+        for (int q = 0; q < P; ++q) {
+          e[k][q] = exp_pair(e[k][q], negm, log2e);
+          acc[q & 1] = add2(acc[q & 1], e[k][q]);
+        }
+      }
+    }
+    const float ws = warp_sum((acc[0].x + acc[1].x) + (acc[0].y + acc[1].y));
+    if (lane == 0) rbuf[warp].s = ws;
+    __syncthreads();
+    float sum = rbuf[0].s;
+#pragma unroll
+    for (int w = 1; w < NW; ++w) sum += rbuf[w].s;
+    const float2 inv = dup2(1.0f / sum);
+    char* yrow = static_cast<char*>(p.y) + row * static_cast<int64_t>(row_bytes);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (ok[k]) {
+#pragma unroll
+        for (int q = 0; q < P; ++q) e[k][q] = mul2(e[k][q], inv);
+        st_stream_v4(yrow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::from_pairs(e[k]));
       }
     }
   }
