@@ -85,13 +85,18 @@ def test_shapes(dtype, H):
     check(case, dtype, out, f"37x{H} {dtype} {p}")
 
 
+# rows enough that every CTA (warp, for H <= 1024) walks several rows, so the
+# ring wraps (slot back to 0, mbarrier phase flipped) at every depth
+RING_ROWS = {"tiny_64x768_fp32": 64, "cancel_65536x1000_bf16": 8000,
+             "pages_2048x4096_fp16": 2048, "large_32768x8192_bf16": 912}
+
+
 @pytest.mark.parametrize("stages", [1, 2, 3, 4])
-@pytest.mark.parametrize("name", ["tiny_64x768_fp32", "cancel_65536x1000_bf16",
-                                  "pages_2048x4096_fp16", "large_32768x8192_bf16"])
+@pytest.mark.parametrize("name", sorted(RING_ROWS))
 def test_ring_depths(name, stages):
     # the staging ring's depth changes only the launch, never the grid (so the
     # workspace size is the same for every depth)
-    w = synth.with_rows(synth.get(name), 150)
+    w = synth.with_rows(synth.get(name), RING_ROWS[name])
     case = make_case(w, seed=5)
     prev = mba.addln_set_cta_shape(0, stages)
     try:
