@@ -489,11 +489,13 @@ def run_ours(args):
 
 
 def run_e2e(mba, w, d, dev, steps, W, barrier, ws):
-    """Public API with host buffers: every step copies X, R, gamma, beta from
-    pinned host memory, runs the fused call, and reads the outputs back into
-    pinned host memory.  For Add+LayerNorm the step is one
-    add_layernorm_fwd_host call (the C ABI with host buffers, copies inside,
-    chunks pipelined over both copy directions); the other ops copy around
+    """Public API with host buffers: every step moves X, R, gamma, beta from
+    pinned host memory to the GPU, runs the fused call, and moves the outputs
+    back into pinned host memory.  For Add+LayerNorm the step is one
+    add_layernorm_fwd_host call (the C ABI with host buffers): the kernel reads
+    and writes the pinned buffers in place over the host link when the GPU can
+    reach host memory (mapped mode), else chunks are copied, pipelined over
+    both copy directions; the line records which.  The other ops copy around
     their device-buffer call on one stream."""
     soft = w.op == "softmax"
     hx = d["x"].pin_memory()
@@ -563,13 +565,24 @@ def run_e2e(mba, w, d, dev, steps, W, barrier, ws):
         (hx.numel() + hr.numel()) * hx.element_size() + \
         (4 if w.op == "bias_gelu_residual" else 8) * w.H
     d2h = hy.numel() * hy.element_size() * (2 if w.want_resid else 1) + (8 * w.rows if w.want_stats else 0)
-    return {"value": round(whole_job_gbs(ws, w.algorithmic_bytes(), steps, el), 2), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": round(el / steps * 1e3, 4),
-            "note": ("add_layernorm_fwd_host (C ABI, host buffers, pinned): copies inside the "
-                     "call, 4 MiB row chunks pipelined over H2D, kernel and D2H streams"
-                     if host_ws is not None else
-                     f"{w.op} with pinned host buffers; H2D, kernel, D2H on one stream")}
+    mode = None
+    if host_ws is not None:
+        mode = {mba.binding.HOST_MAPPED: "mapped", mba.binding.HOST_PIPELINED: "pipelined"}.get(
+            mba.add_layernorm_fwd_host_last_mode(), "unknown")
+    notes = {
+        "mapped": ("add_layernorm_fwd_host (C ABI, pinned host buffers), mapped mode: gamma and "
+                   "beta copied to the GPU, then the kernel reads X, R and writes the outputs in "
+                   "place in host memory over the host link, both directions at once"),
+        "pipelined": ("add_layernorm_fwd_host (C ABI, pinned host buffers), pipelined mode: "
+                      "4 MiB row chunks copied over H2D, kernel and D2H streams"),
+    }
+    out = {"value": round(whole_job_gbs(ws, w.algorithmic_bytes(), steps, el), 2), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+           "ms_per_step": round(el / steps * 1e3, 4),
+           "note": notes.get(mode, f"{w.op} with pinned host buffers; H2D, kernel, D2H on one stream")}
+    if mode is not None:
+        out["mode"] = mode
+    return out
 
 
 # ------------------------------------------------------- CPU oracle arm

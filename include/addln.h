@@ -108,12 +108,21 @@ int add_layernorm_fwd(const void *x, const void *r, const float *gamma, const fl
  *   stream                the caller's stream; the kernels run on it, and it
  *                         waits for the last copy back, so synchronising it
  *                         completes the call
- * Rows go through in chunks of about 4 MiB of X, pipelined over a copy-in
- * stream, `stream` and a copy-out stream (created once per device on the
- * first call, which should come before any stream capture), so both copy
- * directions and the kernels overlap; each copy is one cudaMemcpyAsync.
- * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
- * the copies to run asynchronously; pageable memory is correct but slower.
+ * Two ways, chosen per call (add_layernorm_fwd_host_last_mode reports which):
+ *   mapped   when the device can reach host memory (the pageable memory
+ *            access attribute, as on coherent CPU-GPU links), every row
+ *            buffer and output is page-locked memory mapped into the device's
+ *            address space (cudaHostAlloc / cudaHostRegister), and rows are
+ *            16-byte aligned: gamma and beta are copied to the workspace and
+ *            the kernel reads X, R and writes the outputs in place over the
+ *            host link, with 16-byte loads and stores only (no bulk copies),
+ *            all on `stream`;
+ *   pipelined otherwise: rows go through in chunks of about 4 MiB of X,
+ *            pipelined over a copy-in stream, `stream` and a copy-out stream
+ *            (created once per device on the first call, which should come
+ *            before any stream capture), so both copy directions and the
+ *            kernels overlap; each copy is one cudaMemcpyAsync.  Pageable
+ *            host memory is correct here but slower.
  * y_host and resid_out_host may equal x_host or r_host exactly (in place);
  * any other overlap is ADDLN_ERR_ALIAS.  Results are those of
  * add_layernorm_fwd on the same rows.  Errors as add_layernorm_fwd, plus
@@ -129,6 +138,13 @@ int add_layernorm_fwd_host(const void *x_host, const void *r_host, const float *
  * a negative code for an invalid shape or dtype. */
 int64_t add_layernorm_fwd_host_workspace_size(int64_t rows, int64_t H, int dtype, int want_resid,
                                               int want_stats);
+
+/* How the last add_layernorm_fwd_host call that queued work (on any thread)
+ * moved its data: ADDLN_HOST_MAPPED, ADDLN_HOST_PIPELINED, or 0 before any
+ * such call.  A diagnostic for tests and benchmarks. */
+#define ADDLN_HOST_PIPELINED 1
+#define ADDLN_HOST_MAPPED 2
+int add_layernorm_fwd_host_last_mode(void);
 
 /*
  * Unfused baseline, step 1: A = X + R rounded to dtype, elementwise over n

@@ -7,6 +7,7 @@ from .binding import (  # noqa: F401
     AddLNError,
     add_layernorm_fwd,
     add_layernorm_fwd_host,
+    add_layernorm_fwd_host_last_mode,
     add_layernorm_fwd_host_workspace_size,
     add_fwd,
     layernorm_fwd,

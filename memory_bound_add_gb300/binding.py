@@ -37,6 +37,7 @@ SIGNATURES = {
                                               ctypes.c_float, ctypes.c_int, _P, _I64, _P]),
     "add_layernorm_fwd_host_workspace_size": (ctypes.c_int64, [_I64, _I64, ctypes.c_int,
                                                                ctypes.c_int, ctypes.c_int]),
+    "add_layernorm_fwd_host_last_mode": (ctypes.c_int, []),
     "add_fwd": (ctypes.c_int, [_P, _P, _P, _I64, ctypes.c_int, _P]),
     "layernorm_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_float,
                                      ctypes.c_int, _P]),
@@ -195,13 +196,25 @@ def add_layernorm_fwd_host_workspace_size(rows: int, H: int, dtype: int, want_re
     return n
 
 
+HOST_PIPELINED = 1
+HOST_MAPPED = 2
+
+
+def add_layernorm_fwd_host_last_mode() -> int:
+    """HOST_MAPPED or HOST_PIPELINED: how the last add_layernorm_fwd_host call
+    moved its data (0 before any call)."""
+    return int(lib().add_layernorm_fwd_host_last_mode())
+
+
 def add_layernorm_fwd_host(x, r, gamma, beta, y, resid_out=None, mean=None, rstd=None,
                            eps: float = 1e-5, workspace=None, stream=None):
-    """add_layernorm_fwd from host tensors to host tensors (pinned for overlap).
+    """add_layernorm_fwd from host tensors to host tensors.
 
-    The copies to and from the GPU happen inside the call; `workspace` is a
-    CUDA uint8 tensor of at least add_layernorm_fwd_host_workspace_size(...)
-    bytes (allocated here when omitted).  Synchronise `stream` (default: the
+    The host-device traffic happens inside the call: read and written in
+    place by the kernel when every row buffer is pinned and the GPU can reach
+    host memory, else copied in pipelined chunks.  `workspace` is a CUDA uint8
+    tensor of at least add_layernorm_fwd_host_workspace_size(...) bytes
+    (allocated here when omitted).  Synchronise `stream` (default: the
     current stream) before reading the outputs.
     """
     rows, H = _rows_shape(x)

@@ -127,7 +127,10 @@ int device_info(DeviceInfo* out) {
   return ADDLN_OK;
 }
 
-int run_rows(const RowArgs& p, int dtype, void* stream) {
+// allow_tma false: rows longer than 1024 take the CTA kernel with 16-byte
+// loads to registers instead of bulk copies (for rows that live in mapped
+// host memory, which only plain loads and stores touch).
+int run_rows(const RowArgs& p, int dtype, void* stream, bool allow_tma = true) {
   LaunchCtx c;
   c.stream = stream;
   c.grid_cap = g_grid_cap.load(std::memory_order_relaxed);
@@ -148,6 +151,7 @@ int run_rows(const RowArgs& p, int dtype, void* stream) {
     else
       path = vec_ok ? ADDLN_PATH_CTA_TMA : ADDLN_PATH_SCALAR;
   }
+  if (!allow_tma && path == ADDLN_PATH_CTA_TMA) path = ADDLN_PATH_CTA_VEC;
   const char* name = "none";
   int out;
   switch (path) {
@@ -461,3 +465,16 @@ const char* addln_last_cuda_error(void) {
 }
 
 }  // extern "C"
+
+// The fused forward on rows that live in mapped host memory (zero-copy):
+// the same checks and kernels as add_layernorm_fwd, without bulk copies.
+int addln::fwd_rows_mapped(const void* x, const void* r, const float* gamma, const float* beta,
+                           void* y, void* resid_out, float* mean, float* rstd, int64_t rows,
+                           int64_t H, float eps, int dtype, void* stream) {
+  int rc = check_rows_args(x, r, true, gamma, beta, y, resid_out, mean, rstd, rows, H, eps, dtype);
+  if (rc != ADDLN_OK || rows == 0) return rc;
+  RowArgs p{x, r, gamma, beta, y, resid_out, mean, rstd, rows, static_cast<int>(H),
+            static_cast<float>(1.0 / static_cast<double>(H)), eps,
+            g_wait_limit_ns.load(std::memory_order_relaxed)};
+  return run_rows(p, dtype, stream, false);
+}

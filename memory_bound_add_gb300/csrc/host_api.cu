@@ -1,7 +1,15 @@
 // add_layernorm_fwd_host: the fused forward from host buffers to host
-// buffers, with the host-device copies inside the call.
+// buffers, with the host-device traffic inside the call.
 //
-// The rows are cut into chunks of about 4 MiB of X each and pipelined over
+// Mapped (zero-copy): when the device can reach host memory and X, R and
+// every output are mapped page-locked memory with 16-byte aligned rows, the
+// kernel reads and writes them in place over the host link, one pass each
+// way with both directions at once; only gamma and beta are copied to the
+// device first.  Rows over 1024 then take the CTA kernel with 16-byte
+// loads, so no bulk copy ever reads host memory.
+//
+// Pipelined, otherwise: the rows are cut into chunks of about 4 MiB of X
+// each and pipelined over
 // three streams: a copy-in stream (X, R of chunk c into device buffer c % 2),
 // the caller's stream (add_layernorm_fwd on the chunk, once its copy has
 // landed) and a copy-out stream (Y and the optional outputs of chunk c, once
@@ -18,11 +26,13 @@
 // shared by all calls on that device; a mutex serialises the enqueueing, so
 // concurrent calls are correct (they queue behind one another on the shared
 // copy streams).
+#include <atomic>
 #include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "../../include/addln.h"
+#include "launch.h"
 
 namespace {
 
@@ -40,6 +50,7 @@ struct Pipe {
 
 std::mutex g_mu;
 Pipe g_pipe[kMaxDevices];
+std::atomic<int> g_last_mode{0};
 
 int64_t elem_bytes(int dtype) { return dtype == ADDLN_FP32 ? 4 : 2; }
 
@@ -101,6 +112,26 @@ bool apart(const void* a, int64_t na, const void* b, int64_t nb) {
   if (a == nullptr || b == nullptr) return true;
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x + static_cast<uintptr_t>(na) <= y || y + static_cast<uintptr_t>(nb) <= x;
+}
+
+// Device address of the host range [p, p + n) when the device can reach any
+// host address (pageable memory access) and both ends of the range are mapped
+// pinned memory at device addresses n - 1 apart; otherwise nullptr.
+void* mapped_range(const void* p, int64_t n, bool device_reaches_host) {
+  if (!device_reaches_host || p == nullptr || n <= 0) return nullptr;
+  cudaPointerAttributes a{}, b{};
+  const char* last = static_cast<const char*>(p) + (n - 1);
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess ||
+      cudaPointerGetAttributes(&b, last) != cudaSuccess) {
+    cudaGetLastError();  // an unregistered pointer is not an error of this call
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || b.type != cudaMemoryTypeHost || a.devicePointer == nullptr ||
+      b.devicePointer == nullptr)
+    return nullptr;
+  if (static_cast<const char*>(b.devicePointer) - static_cast<const char*>(a.devicePointer) != n - 1)
+    return nullptr;
+  return a.devicePointer;
 }
 
 int check_shape(int64_t rows, int64_t H, int dtype) {
@@ -180,6 +211,43 @@ extern "C" int add_layernorm_fwd_host(const void* x_host, const void* r_host,
       (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
     return ADDLN_ERR_WORKSPACE;
 
+  // Zero-copy: when X, R and every output are mapped pinned host memory with
+  // 16-byte aligned rows, the kernel reads and writes them in place over the
+  // host link (one pass each way, both directions at once, no staging and no
+  // pipeline fill or drain); only gamma and beta are copied to the device
+  // first.  Rows over 1024 then take the CTA kernel with 16-byte loads: no
+  // bulk copy reads host memory.
+  {
+    int dev = 0, reach = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reach, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess)
+      return ADDLN_ERR_CUDA;
+    const int64_t tb = rows * H * elem_bytes(dtype);
+    void* dx = mapped_range(x_host, tb, reach != 0);
+    void* dr = mapped_range(r_host, tb, reach != 0);
+    void* dy = mapped_range(y_host, tb, reach != 0);
+    void* da = want_a ? mapped_range(resid_out_host, tb, reach != 0) : nullptr;
+    void* dm = mean_host ? mapped_range(mean_host, rows * 4, reach != 0) : nullptr;
+    void* ds = rstd_host ? mapped_range(rstd_host, rows * 4, reach != 0) : nullptr;
+    auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    const bool all = dx && dr && dy && (!want_a || da) && (!mean_host || dm) && (!rstd_host || ds);
+    if (all && (H * elem_bytes(dtype)) % 16 == 0 && a16(dx) && a16(dr) && a16(dy) &&
+        (!da || a16(da))) {
+      cudaStream_t s = static_cast<cudaStream_t>(stream);
+      char* ws = static_cast<char*>(workspace);
+      if (cudaMemcpyAsync(ws + L.gamma, gamma_host, H * 4, cudaMemcpyHostToDevice, s) !=
+              cudaSuccess ||
+          cudaMemcpyAsync(ws + L.beta, beta_host, H * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return ADDLN_ERR_CUDA;
+      const int out = addln::fwd_rows_mapped(
+          dx, dr, reinterpret_cast<const float*>(ws + L.gamma),
+          reinterpret_cast<const float*>(ws + L.beta), dy, da, static_cast<float*>(dm),
+          static_cast<float*>(ds), rows, H, eps, dtype, stream);
+      if (out == ADDLN_OK) g_last_mode.store(ADDLN_HOST_MAPPED, std::memory_order_relaxed);
+      return out;
+    }
+  }
+
   std::lock_guard<std::mutex> guard(g_mu);
   Pipe* pp = nullptr;
   rc = pipe_of_current_device(&pp);
@@ -234,5 +302,11 @@ extern "C" int add_layernorm_fwd_host(const void* x_host, const void* r_host,
   cudaEventRecord(P.drained[last], P.out);
   if (cudaStreamWaitEvent(s, P.drained[last], 0) != cudaSuccess) ok = false;
   if (rc != ADDLN_OK) return rc;
-  return ok ? ADDLN_OK : ADDLN_ERR_CUDA;
+  if (!ok) return ADDLN_ERR_CUDA;
+  g_last_mode.store(ADDLN_HOST_PIPELINED, std::memory_order_relaxed);
+  return ADDLN_OK;
+}
+
+extern "C" int add_layernorm_fwd_host_last_mode(void) {
+  return g_last_mode.load(std::memory_order_relaxed);
 }

@@ -60,6 +60,12 @@ int launch_cta_row(int dtype, bool tma, const RowArgs& p, const LaunchCtx& c,
 // One CTA per row, element-wise loads, any alignment, H <= max.
 int launch_cta_scalar(int dtype, const RowArgs& p, const LaunchCtx& c, const char** path_name);
 
+// add_layernorm_fwd on rows in mapped host memory: plain 16-byte loads and
+// stores only (no bulk copies); gamma and beta should be device memory.
+int fwd_rows_mapped(const void* x, const void* r, const float* gamma, const float* beta, void* y,
+                    void* resid_out, float* mean, float* rstd, int64_t rows, int64_t H, float eps,
+                    int dtype, void* stream);
+
 // A = X + R over n elements.
 int launch_add(int dtype, const void* x, const void* r, void* a, int64_t n, const LaunchCtx& c);
 

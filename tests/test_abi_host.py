@@ -44,6 +44,7 @@ def header_defines():
 def test_header_declares_the_expected_entry_points():
     assert header_functions() == sorted([
         "add_layernorm_fwd", "add_layernorm_fwd_host", "add_layernorm_fwd_host_workspace_size",
+        "add_layernorm_fwd_host_last_mode",
         "add_fwd", "layernorm_fwd", "softmax_fwd", "bias_gelu_residual_fwd",
         "bias_add_fwd", "gelu_fwd", "add_layernorm_bwd", "add_layernorm_bwd_workspace_size",
         "add_layernorm_bwd_noalloc",
@@ -75,6 +76,8 @@ def test_binding_signatures_cover_the_header():
         assert getattr(binding, "ERR_" + k) == d["ADDLN_ERR_" + k]
     for k in ("AUTO", "WARP_VEC", "CTA_TMA", "CTA_VEC", "SCALAR"):
         assert getattr(binding, "PATH_" + k) == d["ADDLN_PATH_" + k]
+    for k in ("PIPELINED", "MAPPED"):
+        assert getattr(binding, "HOST_" + k) == d["ADDLN_HOST_" + k]
 
 
 def test_strerror_and_limits(lib):

@@ -1,7 +1,9 @@
-"""add_layernorm_fwd_host (host buffers in and out, copies inside the call):
-the same results as add_layernorm_fwd on device buffers, bit for bit, over
-chunkings with a ragged last chunk, every output combination, pageable and
-page-locked memory and in-place use; and the oracle on one case."""
+"""add_layernorm_fwd_host (host buffers in and out, the traffic inside the
+call): the same results as add_layernorm_fwd on device buffers, bit for bit,
+in both of its modes (mapped: page-locked buffers read and written in place by
+the kernel; pipelined: chunked copies, with a ragged last chunk), every output
+combination, misaligned rows and in-place use; which mode each call takes; and
+the oracle on one case."""
 from __future__ import annotations
 
 import pytest
@@ -57,13 +59,31 @@ CASES = [
 ]
 
 
+def device_reaches_host_memory():
+    """cudaDevAttrPageableMemoryAccess of the current device, through the CUDA
+    runtime this process already loaded (None when it cannot be asked)."""
+    import ctypes
+    try:
+        paths = sorted({ln.split()[-1] for ln in open("/proc/self/maps") if "libcudart.so" in ln})
+        rt = ctypes.CDLL(paths[0])
+    except (OSError, IndexError):
+        return None
+    dev, v = ctypes.c_int(0), ctypes.c_int(0)
+    if rt.cudaGetDevice(ctypes.byref(dev)) != 0:
+        return None
+    if rt.cudaDeviceGetAttribute(ctypes.byref(v), 88, dev) != 0:  # PageableMemoryAccess
+        return None
+    return v.value != 0
+
+
 @pytest.mark.parametrize("name,rows", CASES)
 @pytest.mark.parametrize("want_a,want_stats", [(False, False), (True, True)])
-def test_matches_device_entry_point_bitwise(name, rows, want_a, want_stats):
+@pytest.mark.parametrize("pin", [True, False])
+def test_matches_device_entry_point_bitwise(name, rows, want_a, want_stats, pin):
     w = synth.with_rows(synth.get(name), rows)
     d = synth.make_inputs(w, seed=21)
     ref = device_reference(d, want_a, want_stats)
-    got = host_call(d, want_a, want_stats)
+    got = host_call(d, want_a, want_stats, pin=pin)
     for u, v in zip(got, ref):
         assert (u is None) == (v is None)
         if u is not None:
@@ -76,6 +96,31 @@ def test_pageable_memory_and_in_place():
     ref = device_reference(d, False, False)
     assert torch.equal(host_call(d, False, False, pin=False)[0], ref[0])
     assert torch.equal(host_call(d, False, False, in_place=True)[0], ref[0])
+
+
+def test_mode_reports_the_path_taken():
+    w = synth.with_rows(synth.get("pages_2048x4096_fp16"), 600)
+    d = synth.make_inputs(w, seed=25)
+    ref = device_reference(d, True, True)
+    host_call(d, True, True, pin=False)
+    assert mba.add_layernorm_fwd_host_last_mode() == mba.binding.HOST_PIPELINED
+    got = host_call(d, True, True, pin=True)
+    reach = device_reaches_host_memory()
+    mode = mba.add_layernorm_fwd_host_last_mode()
+    if reach is not None:
+        assert mode == (mba.binding.HOST_MAPPED if reach else mba.binding.HOST_PIPELINED)
+    assert all(torch.equal(u, v) for u, v in zip(got, ref))
+    # page-locked rows that are not 16-byte aligned never go mapped
+    n = w.rows * w.H
+    bx = torch.empty(n + 8, dtype=d["x"].dtype).pin_memory()
+    by = torch.empty(n + 8, dtype=d["x"].dtype).pin_memory()
+    hx = bx[1:1 + n].view(w.rows, w.H)
+    hx.copy_(d["x"])
+    hy = by[1:1 + n].view(w.rows, w.H)
+    mba.add_layernorm_fwd_host(hx, d["r"].pin_memory(), d["gamma"], d["beta"], hy, eps=d["eps"])
+    torch.cuda.synchronize()
+    assert mba.add_layernorm_fwd_host_last_mode() == mba.binding.HOST_PIPELINED
+    assert torch.equal(hy, ref[0])
 
 
 def test_mean_without_rstd():
