@@ -478,3 +478,5 @@ int addln::fwd_rows_mapped(const void* x, const void* r, const float* gamma, con
             g_wait_limit_ns.load(std::memory_order_relaxed)};
   return run_rows(p, dtype, stream, false);
 }
+
+bool addln::pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }

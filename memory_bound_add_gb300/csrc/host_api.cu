@@ -4,8 +4,8 @@
 // Mapped (zero-copy): when the device can reach host memory and X, R and
 // every output are mapped page-locked memory with 16-byte aligned rows, the
 // kernel reads and writes them in place over the host link, one pass each
-// way with both directions at once; only gamma and beta are copied to the
-// device first.  Rows over 1024 then take the CTA kernel with 16-byte
+// way with both directions at once; only gamma and beta go to the device
+// first (a small kernel when they are mapped too, else two copies).  Rows over 1024 then take the CTA kernel with 16-byte
 // loads, so no bulk copy ever reads host memory.
 //
 // Pipelined, otherwise: the rows are cut into chunks of about 4 MiB of X
@@ -32,6 +32,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/addln.h"
+#include "common.cuh"
 #include "launch.h"
 
 namespace {
@@ -132,6 +133,20 @@ void* mapped_range(const void* p, int64_t n, bool device_reaches_host) {
   if (static_cast<const char*>(b.devicePointer) - static_cast<const char*>(a.devicePointer) != n - 1)
     return nullptr;
   return a.devicePointer;
+}
+
+// gamma and beta from mapped host memory into the workspace: one small
+// kernel instead of two copies, chained to the row kernel that reads them by
+// programmatic dependent launch (it waits for the work queued before it,
+// which may still be reading the workspace, before it writes).
+__global__ void k_params_in(const float* g, const float* b, float* gd, float* bd, int H) {
+  addln::pdl_trigger();
+  addln::pdl_wait();
+  const int step = gridDim.x * blockDim.x;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < H; i += step) {
+    gd[i] = g[i];
+    bd[i] = b[i];
+  }
 }
 
 int check_shape(int64_t rows, int64_t H, int dtype) {
@@ -235,14 +250,24 @@ extern "C" int add_layernorm_fwd_host(const void* x_host, const void* r_host,
         (!da || a16(da))) {
       cudaStream_t s = static_cast<cudaStream_t>(stream);
       char* ws = static_cast<char*>(workspace);
-      if (cudaMemcpyAsync(ws + L.gamma, gamma_host, H * 4, cudaMemcpyHostToDevice, s) !=
-              cudaSuccess ||
-          cudaMemcpyAsync(ws + L.beta, beta_host, H * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      float* gd = reinterpret_cast<float*>(ws + L.gamma);
+      float* bd = reinterpret_cast<float*>(ws + L.beta);
+      const void* dg = mapped_range(gamma_host, H * 4, true);
+      const void* db = mapped_range(beta_host, H * 4, true);
+      if (dg && db) {
+        constexpr int kThreads = 256;
+        const int blocks = static_cast<int>((H + kThreads - 1) / kThreads);
+        if (addln::launch_kernel(k_params_in, dim3(blocks), dim3(kThreads), 0, s,
+                                 addln::pdl_enabled(), static_cast<const float*>(dg),
+                                 static_cast<const float*>(db), gd, bd,
+                                 static_cast<int>(H)) != cudaSuccess)
+          return ADDLN_ERR_LAUNCH;
+      } else if (cudaMemcpyAsync(gd, gamma_host, H * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+                 cudaMemcpyAsync(bd, beta_host, H * 4, cudaMemcpyHostToDevice, s) != cudaSuccess) {
         return ADDLN_ERR_CUDA;
-      const int out = addln::fwd_rows_mapped(
-          dx, dr, reinterpret_cast<const float*>(ws + L.gamma),
-          reinterpret_cast<const float*>(ws + L.beta), dy, da, static_cast<float*>(dm),
-          static_cast<float*>(ds), rows, H, eps, dtype, stream);
+      }
+      const int out = addln::fwd_rows_mapped(dx, dr, gd, bd, dy, da, static_cast<float*>(dm),
+                                             static_cast<float*>(ds), rows, H, eps, dtype, stream);
       if (out == ADDLN_OK) g_last_mode.store(ADDLN_HOST_MAPPED, std::memory_order_relaxed);
       return out;
     }

@@ -60,6 +60,9 @@ int launch_cta_row(int dtype, bool tma, const RowArgs& p, const LaunchCtx& c,
 // One CTA per row, element-wise loads, any alignment, H <= max.
 int launch_cta_scalar(int dtype, const RowArgs& p, const LaunchCtx& c, const char** path_name);
 
+// Whether launches use programmatic dependent launch (knob addln_set_pdl).
+bool pdl_enabled();
+
 // add_layernorm_fwd on rows in mapped host memory: plain 16-byte loads and
 // stores only (no bulk copies); gamma and beta should be device memory.
 int fwd_rows_mapped(const void* x, const void* r, const float* gamma, const float* beta, void* y,
