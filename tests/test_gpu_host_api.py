@@ -109,6 +109,9 @@ def test_mode_reports_the_path_taken():
     mode = mba.add_layernorm_fwd_host_last_mode()
     if reach is not None:
         assert mode == (mba.binding.HOST_MAPPED if reach else mba.binding.HOST_PIPELINED)
+    if mode == mba.binding.HOST_MAPPED:
+        # rows in host memory are read by 16-byte loads, never by bulk copies
+        assert mba.addln_last_path().startswith("cta_vec"), mba.addln_last_path()
     assert all(torch.equal(u, v) for u, v in zip(got, ref))
     # page-locked rows that are not 16-byte aligned never go mapped
     n = w.rows * w.H
