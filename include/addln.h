@@ -116,7 +116,8 @@ int add_layernorm_fwd(const void *x, const void *r, const float *gamma, const fl
  *            16-byte aligned: gamma and beta are copied to the workspace and
  *            the kernel reads X, R and writes the outputs in place over the
  *            host link, with 16-byte loads and stores only (no bulk copies),
- *            all on `stream`;
+ *            all on `stream` (kernels and at most two copies: the call can
+ *            be captured into a CUDA graph);
  *   pipelined otherwise: rows go through in chunks of about 4 MiB of X,
  *            pipelined over a copy-in stream, `stream` and a copy-out stream
  *            (created once per device on the first call, which should come

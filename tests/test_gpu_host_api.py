@@ -126,6 +126,42 @@ def test_mode_reports_the_path_taken():
     assert torch.equal(hy, ref[0])
 
 
+def test_mapped_mode_captures_into_a_graph():
+    # mapped mode queues kernels only (gamma and beta mapped too), so a call
+    # can be captured and replayed; replays follow the inputs' current values
+    if device_reaches_host_memory() is not True:
+        pytest.skip("the device cannot reach host memory: no mapped mode")
+    w = synth.with_rows(synth.get("pages_2048x4096_fp16"), 1000)
+    d = synth.make_inputs(w, seed=26)
+    d2 = synth.make_inputs(w, seed=27)
+    hx, hr, hg, hb = [d[k].clone().pin_memory() for k in ("x", "r", "gamma", "beta")]
+    hy, ha = torch.empty_like(hx).pin_memory(), torch.empty_like(hx).pin_memory()
+    hm, hs = torch.empty(w.rows).pin_memory(), torch.empty(w.rows).pin_memory()
+    ws = torch.empty(mba.add_layernorm_fwd_host_workspace_size(w.rows, w.H, mba.FP16, True, True),
+                     dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    call = lambda: mba.add_layernorm_fwd_host(hx, hr, hg, hb, hy, ha, hm, hs, eps=d["eps"],
+                                              workspace=ws, stream=s)
+    with torch.cuda.stream(s):
+        call()
+    s.synchronize()
+    assert mba.add_layernorm_fwd_host_last_mode() == mba.binding.HOST_MAPPED
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for t in (hy, ha, hm, hs):
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert all(torch.equal(u, v) for u, v in zip((hy, ha, hm, hs), device_reference(d, True, True)))
+    for k, t in (("x", hx), ("r", hr)):
+        t.copy_(d2[k])
+    g.replay()
+    torch.cuda.synchronize()
+    d2["gamma"], d2["beta"] = d["gamma"], d["beta"]
+    assert all(torch.equal(u, v) for u, v in zip((hy, ha, hm, hs), device_reference(d2, True, True)))
+
+
 def test_mean_without_rstd():
     w = synth.with_rows(synth.get("cancel_65536x1000_bf16"), 3000)
     d = synth.make_inputs(w, seed=23)
