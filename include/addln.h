@@ -19,7 +19,9 @@
  * Conventions shared by every entry point:
  *  - Pointers to tensors are caller-owned DEVICE pointers (cudaMalloc or any
  *    allocator, e.g. PyTorch's).  The library never allocates, frees or
- *    synchronises inside the compute calls; it only enqueues kernels.
+ *    synchronises inside the compute calls; it only enqueues kernels.  The
+ *    one exception is add_layernorm_fwd_host, which takes HOST pointers and
+ *    also queues copies (its own entry below says how).
  *  - Layout: X, R, Y, A are contiguous row-major [rows, H] (row stride H) in
  *    the I/O dtype; gamma, beta are fp32 [H]; mean, rstd are fp32 [rows].
  *  - dtype: ADDLN_FP32, ADDLN_FP16 or ADDLN_BF16 (IEEE binary32, binary16,
@@ -164,13 +166,16 @@ int layernorm_fwd(const void *a, const float *gamma, const float *beta, void *y,
 
 /*
  * Fused row softmax ("算子融合与Kernel合并" 4.3, fused_softmax: a max reduce,
- * an exp-sum reduce and a divide, here in one pass over the row):
+ * an exp-sum reduce and a divide, here with one read of the row from memory
+ * and one write):
  *     Y_ij = exp(X_ij - max_j X_ij) / sum_k exp(X_ik - max_j X_ij)
  *   x  [rows, H] input in dtype (required)
  *   y  [rows, H] output in dtype (required); may be x exactly (in place)
- * Arithmetic in fp32 with the hardware exponential (CUDA's __expf): relative
- * error below 1e-5 wherever the result exceeds 1e-30; Y rounded to nearest
- * even.  Same conventions and error codes as add_layernorm_fwd.
+ * Arithmetic in fp32 with the hardware base-2 exponential (exp(d) as
+ * 2^(d log2 e), results below 2^-126 flushed to zero; CUDA's __expf on rows
+ * that are not 16-byte aligned): relative error below 1e-5 wherever the
+ * result exceeds 1e-30; Y rounded to nearest even.  Same conventions and
+ * error codes as add_layernorm_fwd.
  */
 int softmax_fwd(const void *x, void *y, int64_t rows, int64_t H, int dtype, void *stream);
 
