@@ -151,6 +151,7 @@ def host_fused(lib, x=BASE, r=BASE + 0x1000000, g=BASE + 0x2000000, bt=BASE + 0x
 def test_host_entry_validation_before_any_cuda_call(lib):
     # every rejection below is decided on the host, before the first CUDA call
     from memory_bound_add_gb300 import binding as b
+    mode0 = lib.add_layernorm_fwd_host_last_mode()
     assert host_fused(lib, dtype=3) == b.ERR_DTYPE
     assert host_fused(lib, H=0) == b.ERR_SHAPE
     assert host_fused(lib, rows=-1) == b.ERR_SHAPE
@@ -176,6 +177,8 @@ def test_host_entry_validation_before_any_cuda_call(lib):
     assert lib.add_layernorm_fwd_host_workspace_size(2048, 4096, b.FP16, 0, 1) > base
     # two 512-row chunk buffers of X, R, Y (4 MiB each) plus gamma and beta
     assert base == 2 * 3 * 512 * 4096 * 2 + 2 * 4096 * 4
+    # rejected calls (and rows == 0) record no mode: none queued any work
+    assert lib.add_layernorm_fwd_host_last_mode() == mode0
 
 
 def test_alias_rules(lib):
