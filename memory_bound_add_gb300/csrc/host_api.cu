@@ -229,9 +229,10 @@ extern "C" int add_layernorm_fwd_host(const void* x_host, const void* r_host,
   // Zero-copy: when X, R and every output are mapped pinned host memory with
   // 16-byte aligned rows, the kernel reads and writes them in place over the
   // host link (one pass each way, both directions at once, no staging and no
-  // pipeline fill or drain); only gamma and beta are copied to the device
-  // first.  Rows over 1024 then take the CTA kernel with 16-byte loads: no
-  // bulk copy reads host memory.
+  // pipeline fill or drain); only gamma and beta go to the device first (by
+  // k_params_in when they are mapped too, else by two copies).  Rows over
+  // 1024 then take the CTA kernel with 16-byte loads: no bulk copy reads host
+  // memory.
   {
     int dev = 0, reach = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
