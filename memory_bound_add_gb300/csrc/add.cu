@@ -19,6 +19,20 @@ __global__ void __launch_bounds__(kAddThreads) k_add_vec(const void* x, const vo
   const uint4* xv = static_cast<const uint4*>(x);
   const uint4* rv = static_cast<const uint4*>(r);
   uint4* av = static_cast<uint4*>(a);
+  // as the fused kernel does: while the previous kernel may still be
+  // finishing, ask L2 for the 512-byte chunks of X and R this warp reads
+  // first (a hint only; nothing is read before the wait below)
+  if ((threadIdx.x & 31) == 0) {
+    const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kAddThreads * UNROLL + threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int64_t i = w0 + static_cast<int64_t>(u) * kAddThreads;
+      if (i + 32 <= nvec) {
+        prefetch_l2(xv + i, 512u);
+        prefetch_l2(rv + i, 512u);
+      }
+    }
+  }
   pdl_trigger();
   pdl_wait();
   const int64_t step = static_cast<int64_t>(gridDim.x) * kAddThreads * UNROLL;

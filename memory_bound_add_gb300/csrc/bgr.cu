@@ -98,6 +98,20 @@ __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* 
   const uint4* xv = static_cast<const uint4*>(x);
   const uint4* rv = static_cast<const uint4*>(r);
   uint4* yv = static_cast<uint4*>(y);
+  // while the previous kernel may still be finishing, ask L2 for the 512-byte
+  // chunks of X and R this warp reads first (a hint only; nothing is read
+  // before the wait below)
+  if ((threadIdx.x & 31) == 0) {
+    const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kThreads * UNROLL + threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int64_t i = w0 + static_cast<int64_t>(u) * kThreads;
+      if (i + 32 <= nvec) {
+        prefetch_l2(xv + i, 512u);
+        if constexpr (HAS_R) prefetch_l2(rv + i, 512u);
+      }
+    }
+  }
   pdl_trigger();
   pdl_wait();
   const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads * UNROLL;

@@ -282,6 +282,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Ask L2 for [src, src + bytes) (16-byte aligned, a multiple of 16 bytes).  A
+// hint only: it returns nothing and changes no value anyone reads, and since
+// writes from every SM land in L2, a line fetched before another kernel
+// writes it is updated in place, never read stale.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // L2 policy for data read exactly once.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

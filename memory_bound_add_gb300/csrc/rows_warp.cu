@@ -17,12 +17,13 @@ namespace addln {
 constexpr int kWarpCtaThreads = 128;  // 4 rows per CTA
 constexpr int kRowsPerCta = kWarpCtaThreads / 32;
 
-// Register cap a lane: 64 while it holds at most 24 values (four 256-thread
-// CTAs to an SM); above that 80 for 16-bit rows (three), 96 for fp32 ones,
-// whose eight vectors need more addresses (two).  None of them spills.
+// Register cap a lane: 64 while it holds at most 24 values in at most four
+// vectors (eight 128-thread CTAs to an SM); 72 for fp32 rows of six vectors,
+// whose extra addresses need it (seven); above 24 values 80 for 16-bit rows,
+// 96 for fp32 ones.  None of them spills.
 template <int DT, int NV>
 constexpr int warp_row_max_regs() {
-  return NV * Io<DT>::kVec <= 24 ? 64 : DT == kF32 ? 96 : 80;
+  return NV * Io<DT>::kVec <= 24 ? (NV > 4 ? 72 : 64) : DT == kF32 ? 96 : 80;
 }
 
 // Vector path: 16-byte loads, values held as fp32 pairs.  FULL: the row's
@@ -36,12 +37,20 @@ __global__ void __launch_bounds__(kWarpCtaThreads) __maxnreg__((warp_row_max_reg
   constexpr int S = IO::kBytes;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
+  // while the previous kernel may still be finishing, ask L2 for this warp's
+  // row of X and R (a hint only: nothing is read before the wait below, and
+  // a line the previous kernel writes afterwards is updated in L2)
+  const int H = p.H;
+  const int64_t base = row * static_cast<int64_t>(H);  // element offset of the row
+  if (lane == 0 && row < p.rows) {
+    const uint32_t bytes = static_cast<uint32_t>(H) * S;  // whole 16-byte vectors
+    prefetch_l2(static_cast<const char*>(p.x) + base * S, bytes);
+    if (p.r != nullptr) prefetch_l2(static_cast<const char*>(p.r) + base * S, bytes);
+  }
   pdl_trigger();
   pdl_wait();
   if (row >= p.rows) return;  // whole warp leaves together
-  const int H = p.H;
   const int nvec = H / VEC;
-  const int64_t base = row * static_cast<int64_t>(H);  // element offset of the row
 
   bool ok[NV];
 #pragma unroll
