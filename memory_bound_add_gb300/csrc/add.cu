@@ -21,8 +21,10 @@ __global__ void __launch_bounds__(kAddThreads) k_add_vec(const void* x, const vo
   uint4* av = static_cast<uint4*>(a);
   // as the fused kernel does: while the previous kernel may still be
   // finishing, ask L2 for the 512-byte chunks of X and R this warp reads
-  // first (a hint only; nothing is read before the wait below)
-  if ((threadIdx.x & 31) == 0) {
+  // first (a hint only; nothing is read before the wait below), for short
+  // launches (at most eight steps of the grid-stride loop)
+  if ((threadIdx.x & 31) == 0 &&
+      nvec <= 8 * static_cast<int64_t>(gridDim.x) * kAddThreads * UNROLL) {
     const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kAddThreads * UNROLL + threadIdx.x;
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {

@@ -100,8 +100,10 @@ __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* 
   uint4* yv = static_cast<uint4*>(y);
   // while the previous kernel may still be finishing, ask L2 for the 512-byte
   // chunks of X and R this warp reads first (a hint only; nothing is read
-  // before the wait below)
-  if ((threadIdx.x & 31) == 0) {
+  // before the wait below); only for short launches (at most eight steps of
+  // the grid-stride loop), as on long ones it measured slower
+  if ((threadIdx.x & 31) == 0 &&
+      nvec <= 8 * static_cast<int64_t>(gridDim.x) * kThreads * UNROLL) {
     const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kThreads * UNROLL + threadIdx.x;
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
