@@ -277,6 +277,18 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
   const int64_t stride = ROWWARP ? static_cast<int64_t>(gridDim.x) * NW : gridDim.x;
   int64_t row = ROWWARP ? static_cast<int64_t>(blockIdx.x) * NW + warp : blockIdx.x;
 
+  // While the previous kernel may still be finishing, ask L2 for the warp's
+  // chunks of dY and A of the rows its ring stages first (a hint only:
+  // nothing is read before the wait below, and every SM's writes land in
+  // L2); only when each CTA or warp has at most eight rows.
+  if (lane == 0 && chunk_bytes != 0 && p.rows <= 8 * stride)
+    for (int s = 0; s < stages; ++s) {
+      const int64_t rr = row + s * stride;
+      if (rr >= p.rows) break;
+      const int64_t off = rr * static_cast<int64_t>(row_bytes) + chunk_off;
+      prefetch_l2(static_cast<const char*>(p.dy) + off, chunk_bytes);
+      prefetch_l2(static_cast<const char*>(p.a) + off, chunk_bytes);
+    }
   if (tid == 0) {
     for (int i = 0; i < stages * NW; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_mbar_init();
