@@ -181,6 +181,17 @@ def test_host_entry_validation_before_any_cuda_call(lib):
     assert lib.add_layernorm_fwd_host_last_mode() == mode0
 
 
+def test_valid_host_call_without_a_gpu_fails_cleanly(lib):
+    # past every host-side check, the first CUDA call (the device query that
+    # picks the transfer mode) reports the missing GPU as an error code;
+    # no pointer is touched before it
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: the call would run on the placeholder pointers")
+    from memory_bound_add_gb300 import binding as b
+    assert host_fused(lib) == b.ERR_CUDA
+
+
 def test_alias_rules(lib):
     from memory_bound_add_gb300 import binding as b
     rows, H = 4, 8
