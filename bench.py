@@ -48,6 +48,7 @@ METRIC_SOFTMAX = "fused row softmax effective HBM GB/s and % of GB300 peak; rows
 METRIC_BGR = "fused bias+GELU+residual effective HBM GB/s and % of GB300 peak; rows/sec"
 METRICS = {"add_layernorm": METRIC, "softmax": METRIC_SOFTMAX, "bias_gelu_residual": METRIC_BGR}
 DEFAULT_WORKLOAD = "pages_2048x4096_fp16"
+DEFAULT_STEPS = 20
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -55,7 +56,12 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: ~1 s of work)")
+    ap.add_argument("--steps", type=int, default=None,
+                    help=f"timed steps K: one CUDA graph of K launches (default {DEFAULT_STEPS})")
+    ap.add_argument("--replays", type=int, default=0,
+                    help="replays R of the K-launch graph (default: >= 10, enough for ~0.5 s)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other workloads of the method's scope")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
@@ -71,7 +77,6 @@ def parse_args():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--path", type=int, default=0, help="force a kernel path (ADDLN_PATH_*)")
     ap.add_argument("--grid-cap", type=int, default=0)
-    ap.add_argument("--graph-steps", type=int, default=0, help="launches per captured graph")
     ap.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch (1/0)")
     ap.add_argument("--cta-threads", type=int, default=0, help="TMA kernel threads per CTA (tuning)")
     ap.add_argument("--stages", type=int, default=0, help="TMA kernel staged rows per CTA (tuning)")
@@ -142,8 +147,14 @@ def kernel_source_hash():
 
 
 def profiled_traffic(workload, kernel):
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+    """DRAM bytes (read + write) per launch from the committed ncu record of
+    the workload's dominant kernel, or None.  Only a steady-state record
+    counts: consecutive launches over the rotated buffer sets with L2 left
+    alone between them, so that each launch pays the write-back of the
+    output lines the launches before it left dirty in L2.  A single
+    cold-cache launch ends with its own outputs still dirty in L2 and
+    under-counts the writes.  The record must also have been taken on the
+    current forward kernel sources and name the kernel path that ran."""
     path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
     if not os.path.exists(path):
         return None
@@ -156,10 +167,14 @@ def profiled_traffic(workload, kernel):
         return None
     if kernel and kv.get("kernel") and kernel not in kv["kernel"]:
         return None
+    if kv.get("capture") != "steady-state":
+        return None
     try:
-        return int(kv["dram_bytes_per_launch"])
+        n = int(kv["dram_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+    return {"bytes": n, "source": f"profiles/traffic_{workload}.txt (ncu, steady state, "
+                                  f"{kv.get('launches_averaged', '?')} consecutive launches)"}
 
 
 class ClockSampler:
@@ -286,44 +301,168 @@ def unfused_bytes(w):
     return w.unfused_algorithmic_bytes()
 
 
-def capture(step_fn, n_steps, n_sets, offset=0):
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for i in range(n_steps):
-            step_fn((offset + i) % n_sets)
-    return g
+GRAPH_MAX = 2048          # launches per captured CUDA graph
+MIN_REGION_S = 0.5        # replays repeat until the timed region lasts this long
+MAX_REPLAYS = 20000
 
 
-def timed_graph_run(step_fn, K, W, n_sets, graph_steps, barrier):
-    """Warm up W steps, then time exactly K steps replayed from graphs."""
+def pick_sets(K, need, per_set, budget):
+    """Buffer sets for K steps a replay.  When the set count divides K, replay
+    r + 1 starts on the set replay r used K steps earlier, so every step's
+    inputs were last touched n_sets steps (>= 3x L2 of data) before; returns
+    (n_sets, False).  If no such count fits in `budget` bytes, the smallest
+    count that covers 3x L2 and an L2 flush between replays (outside the
+    timed launches): (need, True)."""
+    for n in range(max(1, need), K + 1):
+        if K % n == 0 and n * per_set <= budget:
+            return n, False
+    return need, True
+
+
+def capture_steps(step_fn, K, n_sets):
+    """CUDA graphs that together launch exactly K steps (step i on set
+    i % n_sets), GRAPH_MAX launches at most in one graph."""
+    graphs = []
+    for lo in range(0, K, GRAPH_MAX):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(lo, min(K, lo + GRAPH_MAX)):
+                step_fn(i % n_sets)
+        graphs.append(g)
+    return graphs
+
+
+def timed_graph_run(step_fn, K, W, n_sets, barrier, replays=0, flush=None):
+    """Warm up W steps, capture exactly K steps as CUDA graphs (one graph up
+    to GRAPH_MAX launches), then replay them R times, each replay between
+    its own pair of CUDA events on the launching stream.  R = `replays`, or
+    by default enough replays (at least 10) that the timed region lasts
+    about MIN_REGION_S, so that the clock sampler sees it.  `flush` (a
+    callable) runs between replays, outside their events.
+
+    Returns the median, min, max and mean seconds of one replay (K steps),
+    R, and the wall-clock bounds of the timed region."""
     for i in range(W):
         step_fn(i % n_sets)
     torch.cuda.synchronize()
-    G = min(K, graph_steps)
-    G = max(n_sets, (G // n_sets) * n_sets) if K >= n_sets else K
-    main = capture(step_fn, G, n_sets)
-    rem_n = K % G
-    rem = capture(step_fn, rem_n, n_sets) if rem_n else None
-    main.replay()          # upload the graph; not counted
-    if rem is not None:
-        rem.replay()
-    torch.cuda.synchronize()
+    graphs = capture_steps(step_fn, K, n_sets)
+
+    def replay():
+        for g in graphs:
+            g.replay()
+
     stream = torch.cuda.current_stream()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    replay()                   # upload the graphs; not counted
+    torch.cuda.synchronize()
+    R = replays
+    if R <= 0:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        est = max(e0.elapsed_time(e1) / 1e3, 1e-7)
+        R = int(min(MAX_REPLAYS, max(10, math.ceil(MIN_REGION_S / est))))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(R)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(R)]
     barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    e0.record(stream)
-    for _ in range(K // G):
-        main.replay()
-    if rem is not None:
-        rem.replay()
-    e1.record(stream)
+    for r in range(R):
+        if flush is not None:
+            flush()
+        starts[r].record(stream)
+        replay()
+        ends[r].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     barrier()
-    return e0.elapsed_time(e1) / 1e3, t0, t1
+    times = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
+    return {"median_s": statistics.median(times), "min_s": min(times), "max_s": max(times),
+            "mean_s": sum(times) / R, "replays": R, "t0": t0, "t1": t1}
+
+
+def l2_flusher(dev):
+    """Writes a buffer of twice the L2 size (evicts whatever L2 holds)."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    return lambda: buf.fill_(1)
+
+
+def device_budget(dev):
+    free, _ = torch.cuda.mem_get_info(dev)
+    return int(0.5 * free)
+
+
+def measure_workload(mba, w, d, dev, K, W, barrier, args, unfused=True):
+    """Times the fused call on workload w (and, when asked, its unfused
+    chain) with the same harness: K launches captured in one CUDA graph,
+    replayed R times, the median replay taken.  Inputs rotate over buffer
+    sets holding >= 3x the L2 size.  Returns the raw timings."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    need = max(2, math.ceil(3 * l2 / set_bytes(w)))
+    n_sets, needs_flush = pick_sets(K, need, set_bytes(w), device_budget(dev))
+    sets = make_sets(w, d, n_sets, dev)
+    flush = l2_flusher(dev) if needs_flush else None
+    gamma, beta = d["gamma"].to(dev), d["beta"].to(dev)
+    eps = d["eps"]
+
+    def fused_step(i):
+        s = sets[i]
+        if args.kernel == "add":
+            mba.add_fwd(s["x"], s["r"], s["y"])
+            return
+        if w.op == "softmax":
+            mba.softmax_fwd(s["x"], s["y"])
+            return
+        if w.op == "bias_gelu_residual":
+            mba.bias_gelu_residual_fwd(s["x"], s["r"], beta, s["y"])
+            return
+        mba.add_layernorm_fwd(s["x"], s["r"], gamma, beta, s["y"], s["a"], s["mean"], s["rstd"],
+                              eps=eps)
+
+    def unfused_step(i):
+        s = sets[i]
+        if w.op == "bias_gelu_residual":
+            mba.bias_gelu_residual_unfused(s["x"], s["r"], beta, t=s["t"], y=s["y"])
+            return
+        a = s["a"] if s["a"] is not None else s["y"]
+        mba.add_fwd(s["x"], s["r"], a)
+        mba.layernorm_fwd(a, gamma, beta, s["y"], s["mean"], s["rstd"], eps=eps)
+
+    fused_step(0)
+    torch.cuda.synchronize()
+    path = (mba.addln_last_path() if w.op != "bias_gelu_residual" else "bgr_vec") \
+        if args.kernel == "fused" else "add_vec"
+    if mba.addln_get_device_error() != 0:
+        raise RuntimeError(f"{w.name}: device error word set during warm-up")
+    out = {"n_sets": n_sets, "flush": needs_flush, "path": path,
+           "fused": timed_graph_run(fused_step, K, W, n_sets, barrier, args.replays, flush)}
+    if mba.addln_get_device_error() != 0:
+        raise RuntimeError(f"{w.name}: device error word set during the timed region")
+    if unfused and w.op != "softmax" and args.kernel == "fused":
+        out["unfused"] = timed_graph_run(unfused_step, K, W, n_sets, barrier, args.replays, flush)
+    del sets
+    return out
+
+
+def config_summary(w, m, peak):
+    """One workload's line in the `configs` object."""
+    alg = w.algorithmic_bytes()
+    t = m["fused"]["median_s"] / m["steps"]
+    out = {"us_per_step": round(t * 1e6, 3), "gbs": round(alg / t / 1e9, 1),
+           "frac": round(alg / t / 1e9 / peak, 4),
+           "pct_of_nominal_8TBs": round(100 * alg / t / 1e9 / NOMINAL_HBM_GBS, 2),
+           "rows_per_s": round(w.rows / t, 1), "kernel_path": m["path"],
+           "algorithmic_bytes_per_step": alg,
+           "spread_us": [round(m["fused"]["min_s"] / m["steps"] * 1e6, 3),
+                         round(m["fused"]["max_s"] / m["steps"] * 1e6, 3)],
+           "replays": m["fused"]["replays"]}
+    if "unfused" in m:
+        tu = m["unfused"]["median_s"] / m["steps"]
+        out["unfused_us_per_step"] = round(tu * 1e6, 3)
+        out["fused_speedup"] = round(tu / t, 3)
+    return out
 
 
 def run_ours(args):
@@ -347,65 +486,36 @@ def run_ours(args):
     if args.rows:
         w = synth.with_rows(w, args.rows)
     d = synth.make_inputs(w, seed=replica_seed(args.seed, rank))
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    n_sets = max(2, math.ceil(3 * l2 / set_bytes(w)))
-    sets = make_sets(w, d, n_sets, dev)
-    gamma, beta = d["gamma"].to(dev), d["beta"].to(dev)
-    eps = d["eps"]
     alg = w.algorithmic_bytes()
+    K = args.steps if args.steps else DEFAULT_STEPS
+    W = max(3, args.warmup)
 
     mba.addln_set_force_path(args.path)
     mba.addln_set_grid_cap(args.grid_cap)
     mba.addln_set_pdl(args.pdl)
     mba.addln_set_cta_shape(args.cta_threads, args.stages)
 
-    def fused_step(i):
-        s = sets[i]
-        if args.kernel == "add":
-            mba.add_fwd(s["x"], s["r"], s["y"])
-            return
-        if w.op == "softmax":
-            mba.softmax_fwd(s["x"], s["y"])
-            return
-        if w.op == "bias_gelu_residual":
-            mba.bias_gelu_residual_fwd(s["x"], s["r"], beta, s["y"])
-            return
-        mba.add_layernorm_fwd(s["x"], s["r"], gamma, beta, s["y"], s["a"], s["mean"], s["rstd"],
-                              eps=eps)
-
-    fused_step(0)
-    torch.cuda.synchronize()
-    path = (mba.addln_last_path() if w.op != "bias_gelu_residual" else "bgr_vec") \
-        if args.kernel == "fused" else "add_vec"
-    if mba.addln_get_device_error() != 0:
-        raise RuntimeError("device error word set during warm-up")
-
-    # rough per-step time, to size K for ~1 s when not given
-    t = time.time()
-    for i in range(20):
-        fused_step(i % n_sets)
-    torch.cuda.synchronize()
-    est = (time.time() - t) / 20
-    K = args.steps if args.steps else max(100, int(1.0 / max(est, 1e-6)))
-    W = max(3, args.warmup)
-    graph_steps = args.graph_steps or max(n_sets, min(K, 256))
-
     sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
     if sampler:
         sampler.start()
         time.sleep(0.5)
-    elapsed, t0, t1 = timed_graph_run(fused_step, K, W, n_sets, graph_steps, barrier)
+    want_unfused = not args.only_fused and not args.no_unfused
+    m = measure_workload(mba, w, d, dev, K, W, barrier, args, unfused=want_unfused)
+    m["steps"] = K
     if sampler:
         time.sleep(0.25)
-        sampler.stop()
-    elapsed = max_over_ranks(elapsed, dev)
-    if mba.addln_get_device_error() != 0:
-        raise RuntimeError("device error word set during the timed region")
+    fz = m["fused"]
+    t0, t1 = fz["t0"], fz["t1"]
+    elapsed = max_over_ranks(fz["median_s"], dev)     # one replay: exactly K steps
+    path = m["path"]
 
     value = whole_job_gbs(ws, alg, K, elapsed)
     per_launch_s = elapsed / K
     achieved = alg / per_launch_s / 1e9
     peak, peak_kind = measured_peak()
+    R = fz["replays"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    traffic = profiled_traffic(w.name, path)
     result = {
         "metric": METRICS[w.op],
         "value": round(value, 2),
@@ -426,17 +536,24 @@ def run_ours(args):
             "outputs": "Y" + (", A" if w.want_resid else "") + (", mean, rstd" if w.want_stats else ""),
             "eps": w.eps if w.op != "softmax" else None,
             "algorithmic_bytes_per_step": alg,
-            "l2": f"inputs rotate over {n_sets} buffer sets ({n_sets * set_bytes(w) / 1e6:.0f} MB, "
-                  f">= 3x the {l2 / 1e6:.0f} MB L2)",
-            "graph": f"{graph_steps} launches per CUDA graph",
+            "l2": (f"inputs rotate over {m['n_sets']} buffer sets "
+                   f"({m['n_sets'] * set_bytes(w) / 1e6:.0f} MB, >= 3x the {l2 / 1e6:.0f} MB L2)"
+                   + ("; L2 flushed between replays" if m["flush"] else
+                      "; the set count divides K, so replays continue the rotation")),
+            "timing": (f"the K={K} steps are one CUDA graph of {K} launches, replayed R={R} "
+                       f"times, each replay between its own CUDA events on the launching stream; "
+                       f"value and ms_per_step from the median replay"),
+            "replays": R,
             "kernel_path": path,
             "pdl": bool(args.pdl),
             "parallelism": f"{ws} independent replica(s), no collective on the data path",
         },
+        "ms_per_step_spread": [round(fz["min_s"] / K * 1e3, 6), round(fz["max_s"] / K * 1e3, 6)],
+        "ms_per_step_mean": round(fz["mean_s"] / K * 1e3, 6),
         "rows_per_s": round(ws * w.rows * K / elapsed, 1),
         "pct_of_nominal_8TBs": round(100 * value / ws / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_peak": round(100 * value / ws / peak, 2),
-        "gpu_launches": K,
+        "gpu_launches": R * K,
         "roofline": {
             "bound": "hbm",
             "achieved": round(achieved, 2),
@@ -444,33 +561,49 @@ def run_ours(args):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "peak_kind": f"{peak_kind} copy bandwidth",
-            "traffic": profiled_traffic(w.name, path),
-            "note": "achieved = algorithmic bytes per launch / (timed region / launches); "
-                    "one kernel per step, back to back from a CUDA graph",
+            "traffic": traffic["bytes"] if traffic else None,
+            "note": "achieved = algorithmic bytes per launch / (median replay of K back-to-back "
+                    "launches / K); one kernel per step",
         },
     }
+    if traffic:
+        result["roofline"]["traffic_source"] = traffic["source"]
+        result["roofline"]["traffic_over_algorithmic"] = round(traffic["bytes"] / alg, 4)
 
-    if not args.only_fused and not args.no_unfused and w.op != "softmax":
-        def unfused_step(i):
-            s = sets[i]
-            if w.op == "bias_gelu_residual":
-                mba.bias_gelu_residual_unfused(s["x"], s["r"], beta, t=s["t"], y=s["y"])
-                return
-            a = s["a"] if s["a"] is not None else s["y"]
-            mba.add_fwd(s["x"], s["r"], a)
-            mba.layernorm_fwd(a, gamma, beta, s["y"], s["mean"], s["rstd"], eps=eps)
-        Ku = min(K, 20000)
-        el_u, _, _ = timed_graph_run(unfused_step, Ku, W, n_sets, graph_steps, barrier)
-        el_u = max_over_ranks(el_u, dev)
+    if "unfused" in m:
+        uf = m["unfused"]
+        el_u = max_over_ranks(uf["median_s"], dev)
         result["unfused_baseline"] = {
-            "value": round(ws * alg * Ku / el_u / 1e9, 2),
+            "value": round(ws * alg * K / el_u / 1e9, 2),
             "unit": "GB/s (fused algorithmic bytes / time)",
-            "own_traffic_gbs": round(ws * unfused_bytes(w) * Ku / el_u / 1e9, 2),
-            "ms_per_step": round(el_u / Ku * 1e3, 6),
-            "steps": Ku,
-            "gpu_launches": (3 if w.op == "bias_gelu_residual" else 2) * Ku,
-            "fused_speedup": round(el_u / Ku / (elapsed / K), 3),
+            "own_traffic_gbs": round(ws * unfused_bytes(w) * K / el_u / 1e9, 2),
+            "ms_per_step": round(el_u / K * 1e3, 6),
+            "steps": K,
+            "replays": uf["replays"],
+            "gpu_launches": (3 if w.op == "bias_gelu_residual" else 2) * K * uf["replays"],
+            "fused_speedup": round(el_u / elapsed, 3),
         }
+
+    # every workload of the method's scope, measured the same way in this run
+    if (not args.only_fused and not args.no_configs and not args.rows and w.op == "add_layernorm"
+            and args.kernel == "fused"):
+        configs = {w.name: config_summary(w, m, peak)}
+        for name in synth.PRIMARY:
+            if name == w.name:
+                continue
+            wc = synth.get(name)
+            dc = synth.make_inputs(wc, seed=replica_seed(args.seed, rank))
+            mc = measure_workload(mba, wc, dc, dev, K, W, barrier, args, unfused=want_unfused)
+            mc["steps"] = K
+            for k in ("fused", "unfused"):
+                if k in mc:
+                    mc[k]["median_s"] = max_over_ranks(mc[k]["median_s"], dev)
+            configs[name] = config_summary(wc, mc, peak)
+            del dc
+            torch.cuda.empty_cache()
+        result["configs"] = {n: configs[n] for n in synth.PRIMARY if n in configs}
+    if sampler:
+        sampler.stop()
 
     if not args.only_fused and not args.no_e2e:
         result["e2e"] = run_e2e(mba, w, d, dev, args.e2e_steps, W, barrier, ws)
@@ -774,6 +907,7 @@ def run_chain(args):
     W = max(3, args.warmup)
     stream = torch.cuda.current_stream()
     out = {}
+    finals = {}
     for pdl in (0, 1):
         mba.addln_set_pdl(pdl)
         for _ in range(W):
@@ -786,21 +920,35 @@ def run_chain(args):
         e1.record(stream)
         torch.cuda.synchronize()
         eager = e0.elapsed_time(e1) / 1e3 / (K * L)
+        finals[f"eager_pdl{pdl}"] = bufs[(L - 1) & 1].clone()
+        bufs[(L - 1) & 1].zero_()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             step()
         for _ in range(W):
             graph.replay()
         torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(K):
-            graph.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        graphed = e0.elapsed_time(e1) / 1e3 / (K * L)
+        times = []
+        for _ in range(max(10, args.replays or 10)):
+            e0.record(stream)
+            for _ in range(K):
+                graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) / 1e3 / (K * L))
+        graphed = statistics.median(times)
+        finals[f"graph_pdl{pdl}"] = bufs[(L - 1) & 1].clone()
         out[f"eager_pdl{pdl}_us_per_layer"] = round(eager * 1e6, 3)
         out[f"graph_pdl{pdl}_us_per_layer"] = round(graphed * 1e6, 3)
     mba.addln_set_pdl(1)
+    if mba.addln_get_device_error() != 0:
+        raise RuntimeError("device error word set during the chain")
+    # every mode must leave the same final Y (the oracle comparison of every
+    # layer of such a chain is in the GPU parity tests)
+    ref = finals["eager_pdl0"]
+    same = all(torch.equal(ref, v) for v in finals.values())
+    if not same:
+        raise RuntimeError("the chain's final Y differs between eager, graph and PDL modes")
     best = min(out[k] for k in out) / 1e6
     alg = w.algorithmic_bytes()
     print(json.dumps({
@@ -810,8 +958,10 @@ def run_chain(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "layers_per_step": L, "rows": w.rows, "H": w.H,
                    "io_dtype": w.dtype, "l2": "one layer's working set; no rotation (a chain "
-                   "reads what the previous layer wrote, as a model does)"},
-        "chain": out, "gpu_launches": K * L,
+                   "reads what the previous layer wrote, as a model does)",
+                   "graph_timing": "median of 10 timed runs of K graph replays",
+                   "kernel_source_hash": kernel_source_hash()},
+        "chain": out, "final_y_bitwise_equal_across_modes": same, "gpu_launches": K * L,
     }), flush=True)
 
 
@@ -840,7 +990,10 @@ def run_backward(args):
     gamma, beta = d["gamma"].to(dev), d["beta"].to(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     per_set = 3 * w.rows * w.H * w.elem_bytes
-    n_sets = max(2, math.ceil(3 * l2 / per_set))
+    K = args.steps if args.steps else DEFAULT_STEPS
+    W = max(3, args.warmup)
+    need = max(2, math.ceil(3 * l2 / per_set))
+    n_sets, needs_flush = pick_sets(K, need, per_set, device_budget(dev))
     wsb = mba.add_layernorm_bwd_workspace_size(w.rows, w.H, mba.binding.DTYPE_CODE[d["x"].dtype])
     sets = []
     x, r = d["x"].to(dev), d["r"].to(dev)
@@ -864,15 +1017,10 @@ def run_backward(args):
     step(0)
     torch.cuda.synchronize()
     path = mba.addln_last_path()
-    t = time.time()
-    for i in range(20):
-        step(i % n_sets)
-    torch.cuda.synchronize()
-    est = (time.time() - t) / 20
-    K = args.steps if args.steps else max(100, int(1.0 / max(est, 1e-6)))
-    W = max(3, args.warmup)
-    graph_steps = args.graph_steps or max(n_sets, min(K, 256))
-    elapsed, _, _ = timed_graph_run(step, K, W, n_sets, graph_steps, lambda: None)
+    launches = 2                              # the row kernel, then the column sums
+    run = timed_graph_run(step, K, W, n_sets, lambda: None, args.replays,
+                          l2_flusher(dev) if needs_flush else None)
+    elapsed = run["median_s"]
     mba.addln_set_cta_shape(0, 0)
     if mba.addln_get_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
@@ -887,10 +1035,14 @@ def run_backward(args):
         "config": {"workload": w.name, "rows": w.rows, "H": w.H, "io_dtype": w.dtype,
                    "outputs": "dX, dgamma, dbeta", "kernel_path": path,
                    "algorithmic_bytes_per_step": alg, "workspace_bytes": wsb,
-                   "l2": f"inputs rotate over {n_sets} buffer sets (>= 3x L2)"},
+                   "l2": f"inputs rotate over {n_sets} buffer sets (>= 3x L2)"
+                         + ("; L2 flushed between replays" if needs_flush else ""),
+                   "timing": f"one CUDA graph of K={K} steps replayed R={run['replays']} times; "
+                             "median replay", "replays": run["replays"]},
+        "ms_per_step_spread": [round(run["min_s"] / K * 1e3, 6), round(run["max_s"] / K * 1e3, 6)],
         "rows_per_s": round(w.rows * K / elapsed, 1),
         "pct_of_measured_peak": round(100 * value / peak, 2),
-        "gpu_launches": 2 * K,
+        "gpu_launches": launches * K * run["replays"],
         "roofline": {"bound": "hbm", "achieved": round(value, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(value / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                      "traffic": None},

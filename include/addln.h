@@ -85,7 +85,10 @@ extern "C" {
  *   y           [rows, H] output in dtype (required)
  *   resid_out   [rows, H] output A = X + R rounded to dtype, or NULL
  *   mean, rstd  [rows] fp32 outputs, each independently NULL-able
- *   eps         >= 0, added to the variance inside the square root
+ *   eps         >= 0, added to the variance inside the square root.  eps = 0
+ *               is accepted; a row of zero variance (all sums equal) then has
+ *               rstd = +inf and Y = NaN, the 0/0 the definition gives there
+ *               (mean is still the row's value)
  * Statistics use the unrounded fp32 sum, not A rounded to dtype.
  * Returns ADDLN_OK or a negative code.
  */
@@ -253,9 +256,12 @@ int64_t add_layernorm_bwd_workspace_size(int64_t rows, int64_t H, int dtype);
  * workspace.  The column partials go to a device buffer of
  * ADDLN_NOALLOC_SCRATCH_BYTES (32 MiB) compiled into the library, which every
  * GPU that loads the library keeps until the process exits.  No device memory
- * is allocated by the call.  The first call on each device looks up the
- * buffer's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  A shape whose partials need
+ * is allocated by the call.  The first call on each device that computes
+ * dgamma / dbeta looks up the buffer's device address (cudaGetSymbolAddress)
+ * with that device current, and caches it for the device's current context
+ * (after cudaDeviceReset the new context's address is looked up again); make
+ * that first call before any stream capture.  Argument errors are reported
+ * with the same codes, checked in the same order, as add_layernorm_bwd.  A shape whose partials need
  * more than the buffer (add_layernorm_bwd_workspace_size() >
  * ADDLN_NOALLOC_SCRATCH_BYTES) is rejected with ADDLN_ERR_WORKSPACE before any
  * launch.  All calls on a device share the buffer, which keeps the last call's

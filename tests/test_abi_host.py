@@ -192,6 +192,40 @@ def test_valid_host_call_without_a_gpu_fails_cleanly(lib):
     assert host_fused(lib) == b.ERR_CUDA
 
 
+def bwd_call(lib, fn, dy=BASE, a=BASE + 0x1000000, mean=BASE + 0x2000000,
+             rstd=BASE + 0x2100000, gamma=BASE + 0x2200000, dres=None, dx=BASE + 0x3000000,
+             dg=BASE + 0x4000000, db=BASE + 0x4100000, rows=4, H=8, dtype=0):
+    args = (dy, a, mean, rstd, gamma, dres, dx, dg, db, rows, H, dtype)
+    if fn == "add_layernorm_bwd":
+        return lib.add_layernorm_bwd(*args, BASE + 0x5000000, 1 << 20, None)
+    return lib.add_layernorm_bwd_noalloc(*args, None)
+
+
+@pytest.mark.parametrize("kw", [
+    {"dtype": 3}, {"dtype": -1}, {"H": 0}, {"H": -2}, {"rows": -1}, {"H": 16385},
+    {"H": 32769, "dtype": 2}, {"rows": 1 << 62},
+    {"dg": None},                    # dgamma without dbeta
+    {"db": None},                    # dbeta without dgamma
+    {"rows": 0, "dg": None},         # the pair rule holds for an empty batch too
+    {"rows": 0, "dg": None, "db": None, "dy": None},     # an empty batch is a no-op
+])
+def test_noalloc_backward_returns_the_workspace_entry_points_codes(lib, kw):
+    # the no-alloc entry point checks its arguments as add_layernorm_bwd does,
+    # in the same order, before any CUDA call
+    a = bwd_call(lib, "add_layernorm_bwd", **kw)
+    b = bwd_call(lib, "add_layernorm_bwd_noalloc", **kw)
+    assert a == b, kw
+    assert a <= 0
+
+
+def test_noalloc_backward_null_inputs(lib):
+    from memory_bound_add_gb300 import binding as b
+    # no column sums: add_layernorm_bwd's own NULL checks decide
+    for k in ("dy", "a", "mean", "rstd", "gamma", "dx"):
+        assert bwd_call(lib, "add_layernorm_bwd_noalloc", dg=None, db=None, **{k: None}) == b.ERR_NULL
+        assert bwd_call(lib, "add_layernorm_bwd_noalloc", **{k: None}) == b.ERR_NULL
+
+
 def test_alias_rules(lib):
     from memory_bound_add_gb300 import binding as b
     rows, H = 4, 8

@@ -1,7 +1,8 @@
 """GPU parity of the fused bias + GELU + residual kernel (and of the
 three-kernel chain it replaces) against the fp64 oracle on the same seeded
 inputs: vector and element paths, ragged and misaligned buffers, in place,
-and the full-size workloads on sampled rows."""
+and every row of the full-size workloads, with the correctly rounded
+fraction of 16-bit outputs held to a minimum."""
 from __future__ import annotations
 
 import numpy as np
@@ -10,7 +11,7 @@ import torch
 
 import oracle
 import synth
-from _parity import bgr_violations
+from _parity import Rounding, assert_correctly_rounded, bgr_violations, over_row_chunks
 
 pytestmark = pytest.mark.gpu
 mba = pytest.importorskip("memory_bound_add_gb300")
@@ -35,6 +36,7 @@ def check(d, dtype, y, what, chain=False, rows=None):
         i = tuple(np.argwhere(bad)[0])
         raise AssertionError(f"{what}: {int(bad.sum())} outputs out of bound; first {i}: "
                              f"gpu={y.double().numpy()[i]!r} ref={ref[i]!r}")
+    return ref
 
 
 @pytest.mark.parametrize("name", synth.BGR_NAMES)
@@ -44,7 +46,8 @@ def test_small(name):
     x, r, b = d["x"].cuda(), d["r"].cuda(), d["beta"].cuda()
     y = mba.bias_gelu_residual(x, r, b)
     torch.cuda.synchronize()
-    check(d, w.dtype, y.cpu(), name)
+    ref = check(d, w.dtype, y.cpu(), name)
+    assert_correctly_rounded(y.cpu(), ref, w.dtype, name)
     yu = mba.bias_gelu_residual_unfused(x, r, b)
     torch.cuda.synchronize()
     check(d, w.dtype, yu.cpu(), name + " unfused", chain=True)
@@ -79,11 +82,21 @@ def test_shapes_misaligned_and_in_place(dtype, H):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", synth.BGR_NAMES)
-def test_full_size_sampled_rows(name):
+def test_full_size_every_row(name):
     w = synth.get(name)
     d = synth.make_inputs(w, seed=0)
     y = mba.bias_gelu_residual(d["x"].cuda(), d["r"].cuda(), d["beta"].cuda()).cpu()
-    g = np.random.default_rng(0)
-    rows = np.unique(np.concatenate([np.arange(8), np.arange(w.rows - 8, w.rows),
-                                     g.choice(w.rows, size=min(64, w.rows), replace=False)]))
-    check(d, w.dtype, y, f"{name} full size", rows=rows)
+    what = f"{name} full size"
+
+    def one(lo, hi):
+        rows = slice(lo, hi)
+        ref = check(d, w.dtype, y, f"{what} rows [{lo}, {hi})", rows=rows)
+        rnd = Rounding(w.dtype)
+        rnd.add(y[rows], ref)
+        return rnd
+
+    total = Rounding(w.dtype, what)
+    for r in over_row_chunks(w.rows, w.H, one):
+        for k in ("n", "correct", "above", "below"):
+            setattr(total, k, getattr(total, k) + getattr(r, k))
+    total.check()

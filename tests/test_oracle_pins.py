@@ -218,6 +218,20 @@ def test_constant_row_gives_beta_mean_c_rstd_inv_sqrt_eps():
     assert np.all(o["a"] == c)
 
 
+def test_constant_row_with_eps_zero_is_zero_over_zero():
+    # eps = 0 leaves the definition's (A - mean) / sqrt(var + eps) = 0 / 0 on
+    # a constant row: NaN outputs, rstd = +inf, the mean still exact; other
+    # rows of the same call are unaffected
+    H = 64
+    x = torch.full((2, H), 3.0)
+    x[1] = torch.arange(H, dtype=torch.float32)
+    r = torch.zeros((2, H))
+    o = oracle.oracle_add_layernorm(x, r, torch.ones(H), torch.zeros(H), 0.0, "fp32")
+    assert np.all(np.isnan(o["y"][0])) and o["rstd"][0] == np.inf and o["mean"][0] == 3.0
+    assert np.all(np.isfinite(o["y"][1]))
+    assert math.isclose(o["rstd"][1], 1 / math.sqrt((H * H - 1) / 12), rel_tol=1e-14)
+
+
 def test_h_equals_one_gives_beta():
     x = torch.tensor([[3.5], [-2.0], [7.25]])
     r = torch.tensor([[1.0], [0.5], [-0.25]])
