@@ -306,80 +306,121 @@ MIN_REGION_S = 0.5        # replays repeat until the timed region lasts this lon
 MAX_REPLAYS = 20000
 
 
-def pick_sets(K, need, per_set, budget):
-    """Buffer sets for K steps a replay.  When the set count divides K, replay
-    r + 1 starts on the set replay r used K steps earlier, so every step's
-    inputs were last touched n_sets steps (>= 3x L2 of data) before; returns
-    (n_sets, False).  If no such count fits in `budget` bytes, the smallest
-    count that covers 3x L2 and an L2 flush between replays (outside the
-    timed launches): (need, True)."""
-    for n in range(max(1, need), K + 1):
-        if K % n == 0 and n * per_set <= budget:
+LEAD_STEPS = 2            # untimed steps a replay launches before its K timed ones
+
+
+def pick_sets(launches, need, per_set, budget):
+    """Buffer sets for a replay of `launches` steps.  When the set count
+    divides that number, replay r + 1 starts on the set replay r would have
+    used next, so every step's inputs were last touched n_sets steps (>= 3x
+    L2 of data) before; returns (n_sets, False).  If no such count fits in
+    `budget` bytes, the smallest count that covers 3x L2 and an L2 flush
+    between replays (outside the timed launches): (need, True)."""
+    for n in range(max(1, need), launches + 1):
+        if launches % n == 0 and n * per_set <= budget:
             return n, False
     return need, True
 
 
-def capture_steps(step_fn, K, n_sets):
-    """CUDA graphs that together launch exactly K steps (step i on set
-    i % n_sets), GRAPH_MAX launches at most in one graph."""
+def _timing_event():
+    """A timing event that, recorded during stream capture, becomes an event
+    record node of the graph (None if this PyTorch cannot make one)."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+
+
+def replay_lead(K):
+    """Untimed steps a replay launches before its K timed ones: LEAD_STEPS
+    when the timing events can be recorded inside the graph, else 0."""
+    return LEAD_STEPS if _timing_event() is not None and LEAD_STEPS + K <= GRAPH_MAX else 0
+
+
+def capture_steps(step_fn, K, n_sets, lead=0, events=None):
+    """CUDA graphs that launch `lead` untimed steps and then exactly K steps,
+    step i on set i % n_sets (GRAPH_MAX launches at most in one graph).  With
+    `events` (start, end) the pair is recorded inside the graph, right before
+    the first and right after the last of the K steps."""
     graphs = []
-    for lo in range(0, K, GRAPH_MAX):
+    total = lead + K
+    for lo in range(0, total, GRAPH_MAX):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            for i in range(lo, min(K, lo + GRAPH_MAX)):
+            for i in range(lo, min(total, lo + GRAPH_MAX)):
+                if events is not None and i == lead:
+                    events[0].record()
                 step_fn(i % n_sets)
+            if events is not None and min(total, lo + GRAPH_MAX) == total:
+                events[1].record()
         graphs.append(g)
     return graphs
 
 
 def timed_graph_run(step_fn, K, W, n_sets, barrier, replays=0, flush=None):
-    """Warm up W steps, capture exactly K steps as CUDA graphs (one graph up
-    to GRAPH_MAX launches), then replay them R times, each replay between
-    its own pair of CUDA events on the launching stream.  R = `replays`, or
-    by default enough replays (at least 10) that the timed region lasts
-    about MIN_REGION_S, so that the clock sampler sees it.  `flush` (a
-    callable) runs between replays, outside their events.
+    """Warm up W steps, then replay a CUDA graph R times and time exactly K
+    steps in each replay.
 
-    Returns the median, min, max and mean seconds of one replay (K steps),
-    R, and the wall-clock bounds of the timed region."""
+    The graph launches LEAD_STEPS untimed steps and then the K timed steps,
+    with a pair of timing events recorded inside the graph around the K (so a
+    replay's K steps run as they do inside a longer stream of launches,
+    after a step of the same kernel, and the time excludes the graph's own
+    launch); the host waits for each replay before reading its pair.  Where
+    PyTorch cannot capture events, or for K above GRAPH_MAX, each replay is
+    the K steps alone between events on the stream around it.  R =
+    `replays`, or by default enough replays (at least 10) that the timed
+    region lasts about MIN_REGION_S, so that the clock sampler sees it.
+    `flush` (a callable) runs between replays, outside the timed steps.
+
+    Returns the median, min, max and mean seconds of the K steps of a
+    replay, R, the lead steps a replay launches, and the wall-clock bounds
+    of the timed region."""
     for i in range(W):
         step_fn(i % n_sets)
     torch.cuda.synchronize()
-    graphs = capture_steps(step_fn, K, n_sets)
+    stream = torch.cuda.current_stream()
+    lead = replay_lead(K)
+    inner = (_timing_event(), _timing_event()) if lead else None
+    graphs = capture_steps(step_fn, K, n_sets, lead, inner)
+    outer = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
 
-    def replay():
+    def one():
+        if flush is not None:
+            flush()
+        outer[0].record(stream)
         for g in graphs:
             g.replay()
-
-    stream = torch.cuda.current_stream()
-    replay()                   # upload the graphs; not counted
-    torch.cuda.synchronize()
-    R = replays
-    if R <= 0:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        replay()
-        e1.record(stream)
+        outer[1].record(stream)
         torch.cuda.synchronize()
-        est = max(e0.elapsed_time(e1) / 1e3, 1e-7)
-        R = int(min(MAX_REPLAYS, max(10, math.ceil(MIN_REGION_S / est))))
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(R)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(R)]
+        t_out = outer[0].elapsed_time(outer[1]) / 1e3
+        if inner is None:
+            return t_out
+        t_in = inner[0].elapsed_time(inner[1]) / 1e3
+        if not 0.0 < t_in <= t_out:
+            raise RuntimeError(f"in-graph timing events are inconsistent ({t_in} s of a "
+                               f"{t_out} s replay)")
+        return t_in
+
+    try:
+        est = one()             # uploads the graphs; not counted
+    except RuntimeError:
+        # the events recorded in the graph cannot be timed here: the K steps
+        # alone, between events on the stream, with L2 flushed between
+        # replays (the set rotation was sized for the lead steps too)
+        inner, lead = None, 0
+        graphs = capture_steps(step_fn, K, n_sets)
+        flush = flush or l2_flusher(torch.cuda.current_device())
+        est = one()
+    R = replays if replays > 0 else int(min(MAX_REPLAYS, max(10, math.ceil(MIN_REGION_S / max(est, 1e-7)))))
     barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    for r in range(R):
-        if flush is not None:
-            flush()
-        starts[r].record(stream)
-        replay()
-        ends[r].record(stream)
-    torch.cuda.synchronize()
+    times = [one() for _ in range(R)]
     t1 = time.time()
     barrier()
-    times = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
     return {"median_s": statistics.median(times), "min_s": min(times), "max_s": max(times),
-            "mean_s": sum(times) / R, "replays": R, "t0": t0, "t1": t1}
+            "mean_s": sum(times) / R, "replays": R, "lead": lead, "in_graph_events": inner is not None,
+            "t0": t0, "t1": t1}
 
 
 def l2_flusher(dev):
@@ -401,7 +442,7 @@ def measure_workload(mba, w, d, dev, K, W, barrier, args, unfused=True):
     sets holding >= 3x the L2 size.  Returns the raw timings."""
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     need = max(2, math.ceil(3 * l2 / set_bytes(w)))
-    n_sets, needs_flush = pick_sets(K, need, set_bytes(w), device_budget(dev))
+    n_sets, needs_flush = pick_sets(replay_lead(K) + K, need, set_bytes(w), device_budget(dev))
     sets = make_sets(w, d, n_sets, dev)
     flush = l2_flusher(dev) if needs_flush else None
     gamma, beta = d["gamma"].to(dev), d["beta"].to(dev)
@@ -540,9 +581,12 @@ def run_ours(args):
                    f"({m['n_sets'] * set_bytes(w) / 1e6:.0f} MB, >= 3x the {l2 / 1e6:.0f} MB L2)"
                    + ("; L2 flushed between replays" if m["flush"] else
                       "; the set count divides K, so replays continue the rotation")),
-            "timing": (f"the K={K} steps are one CUDA graph of {K} launches, replayed R={R} "
-                       f"times, each replay between its own CUDA events on the launching stream; "
-                       f"value and ms_per_step from the median replay"),
+            "timing": (f"one CUDA graph launching {fz['lead']} untimed steps, then the K={K} timed "
+                       f"steps between two CUDA timing events recorded inside the graph"
+                       if fz["in_graph_events"] else
+                       f"one CUDA graph of the K={K} steps between CUDA events on the launching "
+                       f"stream") + f"; replayed R={R} times, value and ms_per_step from the "
+                                    f"median replay",
             "replays": R,
             "kernel_path": path,
             "pdl": bool(args.pdl),
@@ -554,6 +598,8 @@ def run_ours(args):
         "pct_of_nominal_8TBs": round(100 * value / ws / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_peak": round(100 * value / ws / peak, 2),
         "gpu_launches": R * K,
+        "gpu_launches_note": "timed launches; each replay also launches "
+                             f"{fz['lead']} untimed lead steps",
         "roofline": {
             "bound": "hbm",
             "achieved": round(achieved, 2),
@@ -584,6 +630,12 @@ def run_ours(args):
             "fused_speedup": round(el_u / elapsed, 3),
         }
 
+    # end to end through the host-buffer entry point, before the other
+    # workloads' large host arrays come and go (the pinned buffers then land
+    # in the host memory nearest the GPU, as in a process that runs only this)
+    if not args.only_fused and not args.no_e2e:
+        result["e2e"] = run_e2e(mba, w, d, dev, args.e2e_steps, W, barrier, ws)
+
     # every workload of the method's scope, measured the same way in this run
     if (not args.only_fused and not args.no_configs and not args.rows and w.op == "add_layernorm"
             and args.kernel == "fused"):
@@ -604,9 +656,6 @@ def run_ours(args):
         result["configs"] = {n: configs[n] for n in synth.PRIMARY if n in configs}
     if sampler:
         sampler.stop()
-
-    if not args.only_fused and not args.no_e2e:
-        result["e2e"] = run_e2e(mba, w, d, dev, args.e2e_steps, W, barrier, ws)
 
     if sampler:
         result["clocks"] = sampler.summary(t0, t1)
@@ -993,7 +1042,7 @@ def run_backward(args):
     K = args.steps if args.steps else DEFAULT_STEPS
     W = max(3, args.warmup)
     need = max(2, math.ceil(3 * l2 / per_set))
-    n_sets, needs_flush = pick_sets(K, need, per_set, device_budget(dev))
+    n_sets, needs_flush = pick_sets(replay_lead(K) + K, need, per_set, device_budget(dev))
     wsb = mba.add_layernorm_bwd_workspace_size(w.rows, w.H, mba.binding.DTYPE_CODE[d["x"].dtype])
     sets = []
     x, r = d["x"].to(dev), d["r"].to(dev)
@@ -1037,8 +1086,9 @@ def run_backward(args):
                    "algorithmic_bytes_per_step": alg, "workspace_bytes": wsb,
                    "l2": f"inputs rotate over {n_sets} buffer sets (>= 3x L2)"
                          + ("; L2 flushed between replays" if needs_flush else ""),
-                   "timing": f"one CUDA graph of K={K} steps replayed R={run['replays']} times; "
-                             "median replay", "replays": run["replays"]},
+                   "timing": (f"one CUDA graph of {run['lead']} untimed and K={K} timed steps "
+                              f"(timing events inside the graph), replayed R={run['replays']} "
+                              "times; median replay"), "replays": run["replays"]},
         "ms_per_step_spread": [round(run["min_s"] / K * 1e3, 6), round(run["max_s"] / K * 1e3, 6)],
         "rows_per_s": round(w.rows * K / elapsed, 1),
         "pct_of_measured_peak": round(100 * value / peak, 2),

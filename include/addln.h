@@ -70,6 +70,7 @@ extern "C" {
 #define ADDLN_ERR_DEVICE_TIMEOUT (-8) /* a kernel's bounded wait on its own copy ran out */
 #define ADDLN_ERR_CUDA (-9)           /* a CUDA runtime call outside a launch failed */
 #define ADDLN_ERR_WORKSPACE (-10)     /* workspace missing, too small or not 16-byte aligned */
+#define ADDLN_ERR_BOUNDS (-11)        /* checked build: a kernel skipped an out-of-bounds access */
 
 /* kernel paths for addln_set_force_path */
 #define ADDLN_PATH_AUTO 0
@@ -287,9 +288,31 @@ int64_t addln_max_hidden(int dtype);
  * on its own TMA copy runs out.
  * Returns ADDLN_OK, ADDLN_ERR_DEVICE_TIMEOUT, or ADDLN_ERR_CUDA if the
  * synchronisation or the read failed.  Rows of a kernel that timed out are
- * left unwritten.
+ * left unwritten.  In the bounds-checked build (see addln_bounds_checked) it
+ * also reads and clears the words in which kernels record the first global
+ * access they skipped for falling outside its buffer, and returns
+ * ADDLN_ERR_BOUNDS if any did (details: addln_bounds_violation).
  */
 int addln_get_device_error(void *stream);
+
+/*
+ * 1 if this library was built with ADDLN_CHECK_BOUNDS defined, else 0.  In
+ * that build every global load, store, bulk copy and L2 prefetch of every
+ * kernel is first tested against the extent of the buffer it addresses
+ * (from the call's rows, H, dtype and grid); an access that would leave its
+ * buffer is skipped, not made, so the context stays usable, and is reported
+ * by addln_get_device_error.  A debugging build: slower, and its outputs are
+ * not valid once a violation was reported.  The normal build compiles every
+ * test away.  No counterpart on the source pages.
+ */
+int addln_bounds_checked(void);
+
+/*
+ * Checked build: the word of the last violation addln_get_device_error
+ * reported (bit 63 set; bits 48..62 the number of the access site in the
+ * kernel sources; bits 0..47 the byte offset that was out of range), or 0.
+ */
+uint64_t addln_bounds_violation(void);
 
 /*
  * Test and benchmark only.  Forces the kernel path of add_layernorm_fwd,

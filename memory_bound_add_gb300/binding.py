@@ -24,6 +24,7 @@ OK = 0
 ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_EPS, ERR_ALIAS = -1, -2, -3, -4, -5
 ERR_LAUNCH, ERR_UNSUPPORTED, ERR_DEVICE_TIMEOUT, ERR_CUDA = -6, -7, -8, -9
 ERR_WORKSPACE = -10
+ERR_BOUNDS = -11
 
 PATH_AUTO, PATH_WARP_VEC, PATH_CTA_TMA, PATH_CTA_VEC, PATH_SCALAR = 0, 1, 2, 3, 4
 
@@ -53,6 +54,8 @@ SIGNATURES = {
     "addln_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "addln_max_hidden": (ctypes.c_int64, [ctypes.c_int]),
     "addln_get_device_error": (ctypes.c_int, [_P]),
+    "addln_bounds_checked": (ctypes.c_int, []),
+    "addln_bounds_violation": (ctypes.c_uint64, []),
     "addln_set_force_path": (ctypes.c_int, [ctypes.c_int]),
     "addln_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "addln_set_grid_cap": (ctypes.c_int64, [ctypes.c_int64]),
@@ -75,22 +78,28 @@ class AddLNError(RuntimeError):
         super().__init__(msg)
 
 
+def load(path: str):
+    """A ctypes handle on the library at `path` with every header signature
+    set (the normal build through lib(); the bounds-checked build's tests
+    load theirs here)."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
 def lib():
     """The loaded library (raises if it has not been built)."""
     global _lib
     if _lib is None:
         with _lock:
             if _lib is None:
-                if not os.path.exists(LIB_PATH):
-                    raise RuntimeError(
-                        f"{LIB_PATH} is missing: build it first "
-                        "(python -c 'import __graft_entry__ as g; g.build()')")
-                handle = ctypes.CDLL(LIB_PATH)
-                for name, (res, args) in SIGNATURES.items():
-                    fn = getattr(handle, name)
-                    fn.restype = res
-                    fn.argtypes = args
-                _lib = handle
+                _lib = load(LIB_PATH)
     return _lib
 
 

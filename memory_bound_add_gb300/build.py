@@ -20,6 +20,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libaddln.so")
+# The bounds-checked debugging build (ADDLN_CHECK_BOUNDS): every kernel tests
+# each global access against its buffer first.  Tests only; never loaded by
+# the package itself.
+CHECKED_DIR = os.path.join(OUT_DIR, "checked")
+CHECKED_LIB = os.path.join(CHECKED_DIR, "libaddln_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
@@ -41,23 +46,26 @@ def _inputs() -> list:
         + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list | None = None) -> str:
-    """Build the library if needed and return its path."""
-    if not force and not extra_flags and up_to_date():
-        return LIB
-    os.makedirs(os.path.join(OUT_DIR, "obj"), exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: list | None = None,
+          checked: bool = False) -> str:
+    """Build the library if needed and return its path.  checked: the
+    bounds-checked debugging build instead (its own objects and library)."""
+    out_dir, lib = (CHECKED_DIR, CHECKED_LIB) if checked else (OUT_DIR, LIB)
+    if not force and not extra_flags and up_to_date(lib):
+        return lib
+    os.makedirs(os.path.join(out_dir, "obj"), exist_ok=True)
     cc = nvcc()
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + list(extra_flags or []) + (["-DADDLN_CHECK_BOUNDS"] if checked else [])
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, "obj", os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, "obj", os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *flags, "-c", src, "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
@@ -68,13 +76,55 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list | None =
 
     with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-cudart", "static", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def ptxas_report(extra_flags: list | None = None) -> dict:
+    """Compiles every translation unit with ptxas's verbose report (the same
+    flags as the library, objects to a scratch folder) and returns, for each
+    kernel (mangled name), its registers, stack frame and spill store / load
+    bytes as the assembler reports them."""
+    import re
+    import tempfile
+    cc = nvcc()
+    flags = NVCC_FLAGS + list(extra_flags or []) + ["-Xptxas", "-v"]
+    with tempfile.TemporaryDirectory() as tmp:
+        def one(src):
+            obj = os.path.join(tmp, os.path.basename(src)[:-3] + ".o")
+            res = subprocess.run([cc, *ARCH, *flags, "-c", src, "-o", obj], capture_output=True,
+                                 text=True)
+            if res.returncode != 0:
+                raise RuntimeError(f"nvcc failed on {src}:\n{res.stdout}\n{res.stderr}")
+            return res.stdout + res.stderr
+
+        with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
+            logs = list(ex.map(one, sources()))
+    out = {}
+    for log in logs:
+        cur = None
+        for line in log.splitlines():
+            m = re.search(r"Function properties for (\S+)", line)
+            if m:
+                cur = m.group(1)
+                out.setdefault(cur, {})
+                continue
+            m = re.search(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads",
+                          line)
+            if m and cur:
+                out[cur].update(stack=int(m.group(1)), spill_stores=int(m.group(2)),
+                                spill_loads=int(m.group(3)))
+                continue
+            m = re.search(r"Used (\d+) registers", line)
+            if m and cur:
+                out[cur]["registers"] = int(m.group(1))
+                cur = None
+    return out
 
 
 if __name__ == "__main__":

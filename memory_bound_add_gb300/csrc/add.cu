@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(kAddThreads) k_add_vec(const void* x, const vo
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int64_t i = w0 + static_cast<int64_t>(u) * kAddThreads;
-      if (i + 32 <= nvec) {
+      if (i + 32 <= nvec && ADDLN_IN(501, i * 16, 512, n * IO::kBytes)) {
         prefetch_l2(xv + i, 512u);
         prefetch_l2(rv + i, 512u);
       }
@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kAddThreads) k_add_vec(const void* x, const vo
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int64_t i = i0 + static_cast<int64_t>(u) * kAddThreads;
-      if (i < nvec) {
+      if (i < nvec && ADDLN_IN(502, i * 16, 16, n * IO::kBytes)) {
         xs[u] = ld_stream_v4(xv + i);
         rs[u] = ld_stream_v4(rv + i);
       }
@@ -58,14 +58,15 @@ __global__ void __launch_bounds__(kAddThreads) k_add_vec(const void* x, const vo
         IO::unpack(rs[u], g);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) f[e] += g[e];
-        st_stream_v4(av + i, IO::pack(f));
+        if (ADDLN_IN(503, i * 16, 16, n * IO::kBytes)) st_stream_v4(av + i, IO::pack(f));
       }
     }
   }
   // tail elements past the last whole vector
   if (blockIdx.x == 0) {
     for (int64_t j = nvec * VEC + threadIdx.x; j < n; j += kAddThreads)
-      IO::store1(a, j, IO::load1(x, j) + IO::load1(r, j));
+      if (ADDLN_IN(504, j * IO::kBytes, IO::kBytes, n * IO::kBytes))
+        IO::store1(a, j, IO::load1(x, j) + IO::load1(r, j));
   }
 }
 
@@ -77,7 +78,8 @@ __global__ void __launch_bounds__(kAddThreads) k_add_scalar(const void* x, const
   pdl_wait();
   const int64_t step = static_cast<int64_t>(gridDim.x) * kAddThreads;
   for (int64_t j = static_cast<int64_t>(blockIdx.x) * kAddThreads + threadIdx.x; j < n; j += step)
-    IO::store1(a, j, IO::load1(x, j) + IO::load1(r, j));
+    if (ADDLN_IN(505, j * IO::kBytes, IO::kBytes, n * IO::kBytes))
+      IO::store1(a, j, IO::load1(x, j) + IO::load1(r, j));
 }
 
 template <int DT>
@@ -110,6 +112,8 @@ static int launch_add_t(const void* x, const void* r, void* a, int64_t n, const 
   if (e != cudaSuccess) note_cuda_error(static_cast<int>(e));
   return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
+
+ADDLN_BOUNDS_READER(read_bounds_add)
 
 int launch_add(int dtype, const void* x, const void* r, void* a, int64_t n, const LaunchCtx& c) {
   switch (dtype) {

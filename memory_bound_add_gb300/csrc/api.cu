@@ -31,6 +31,7 @@ std::atomic<int64_t> g_grid_cap{0};
 std::atomic<int> g_pdl{1};
 std::atomic<int> g_cta_threads{0};
 std::atomic<int> g_stages{0};
+std::atomic<uint64_t> g_bounds_violation{0};
 thread_local const char* g_last_path = "none";
 thread_local int g_last_cuda_error = 0;
 
@@ -418,6 +419,7 @@ const char* addln_strerror(int code) {
     case ADDLN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait on its own copy ran out";
     case ADDLN_ERR_CUDA: return "a CUDA runtime call failed";
     case ADDLN_ERR_WORKSPACE: return "workspace missing, too small or not 16-byte aligned";
+    case ADDLN_ERR_BOUNDS: return "a kernel skipped an access outside its buffer (checked build)";
     default: return "unknown error code";
   }
 }
@@ -435,8 +437,34 @@ int addln_get_device_error(void* stream) {
   int code_bw = 0;
   rc = addln::read_and_clear_bwd_error(&code_bw);
   if (rc != ADDLN_OK) return rc;
+  // checked build: the first out-of-bounds access any kernel met
+  int (*const readers[])(unsigned long long*) = {
+      addln::read_bounds_rows_warp, addln::read_bounds_rows_cta, addln::read_bounds_softmax,
+      addln::read_bounds_bgr,       addln::read_bounds_add,      addln::read_bounds_bwd,
+      addln::read_bounds_host};
+  unsigned long long word = 0;
+  for (auto f : readers) {
+    unsigned long long w = 0;
+    rc = f(&w);
+    if (rc != ADDLN_OK) return rc;
+    if (word == 0) word = w;
+  }
+  if (word != 0) {
+    g_bounds_violation.store(word);
+    return ADDLN_ERR_BOUNDS;
+  }
   return code != 0 ? code : (code_sm != 0 ? code_sm : code_bw);
 }
+
+int addln_bounds_checked(void) {
+#ifdef ADDLN_CHECK_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+uint64_t addln_bounds_violation(void) { return g_bounds_violation.load(); }
 
 int addln_set_force_path(int path) {
   if (path < ADDLN_PATH_AUTO || path > ADDLN_PATH_SCALAR) return ADDLN_ERR_SHAPE;

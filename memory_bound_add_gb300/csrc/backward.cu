@@ -45,6 +45,16 @@ struct BwdArgs {
   uint64_t wait_limit_ns;
 };
 
+// Byte extents of a backward launch's buffers (for ADDLN_IN): a [rows, H]
+// tensor in the I/O dtype, gamma [H], mean / rstd [rows], and the [G][2][H]
+// fp32 workspace partials of a grid of G CTAs.
+__device__ __forceinline__ int64_t bw_rows_bytes(const BwdArgs& p, int elem) {
+  return p.rows * static_cast<int64_t>(p.H) * elem;
+}
+__device__ __forceinline__ int64_t bw_ws_bytes(const BwdArgs& p) {
+  return static_cast<int64_t>(gridDim.x) * 8 * p.H;
+}
+
 template <int VEC>
 __device__ __forceinline__ void load_gamma(const float* g, float (&out)[VEC]) {
 #pragma unroll
@@ -126,21 +136,26 @@ __global__ void __launch_bounds__(THREADS) k_bwd_cta(const BwdArgs p) {
   const int64_t stride = gridDim.x;
   int64_t row = blockIdx.x;
   auto issue = [&](int64_t rr) {
-    mbar_arrive_expect_tx(bar_a, 2u * row_bytes);
     const int64_t off = rr * static_cast<int64_t>(row_bytes);
-    bulk_g2s(s0, static_cast<const char*>(p.dy) + off, row_bytes, bar_a, policy);
-    bulk_g2s(s0 + rb, static_cast<const char*>(p.a) + off, row_bytes, bar_a, policy);
+    const bool okc = ADDLN_IN(601, off, row_bytes, bw_rows_bytes(p, S));
+    mbar_arrive_expect_tx(bar_a, okc ? 2u * row_bytes : 0u);
+    if (okc) {
+      bulk_g2s(s0, static_cast<const char*>(p.dy) + off, row_bytes, bar_a, policy);
+      bulk_g2s(s0 + rb, static_cast<const char*>(p.a) + off, row_bytes, bar_a, policy);
+    }
   };
   if (tid == 0 && row < p.rows) issue(row);
   // mean and rstd of the next row are loaded one row ahead, off the row's
   // critical path
   float mu_n = 0.f, rs_n = 0.f;
-  if (row < p.rows) mu_n = __ldg(p.mean + row), rs_n = __ldg(p.rstd + row);
+  if (row < p.rows && ADDLN_IN(602, 4 * row, 4, 4 * p.rows))
+    mu_n = __ldg(p.mean + row), rs_n = __ldg(p.rstd + row);
 
   for (int64_t it = 0; row < p.rows; ++it, row += stride) {
     const int64_t boff = row * static_cast<int64_t>(row_bytes);
     const float mu = mu_n, rs = rs_n;
-    if (row + stride < p.rows) mu_n = __ldg(p.mean + row + stride), rs_n = __ldg(p.rstd + row + stride);
+    if (row + stride < p.rows && ADDLN_IN(603, 4 * (row + stride), 4, 4 * p.rows))
+      mu_n = __ldg(p.mean + row + stride), rs_n = __ldg(p.rstd + row + stride);
     const bool timed_out = !mbar_wait_bounded(bar_a, static_cast<uint32_t>(it & 1), p.wait_limit_ns);
     uint4 dv[NV];       // dY kept packed; the stage is refilled after the barrier
     float xh[NV][VEC];
@@ -153,7 +168,8 @@ __global__ void __launch_bounds__(THREADS) k_bwd_cta(const BwdArgs p) {
         dv[k] = ld_shared_v4(s0 + c * 16);
         IO::unpack(dv[k], d);
         IO::unpack(ld_shared_v4(s0 + rb + c * 16), xh[k]);
-        load_gamma<VEC>(p.gamma + c * VEC, gg);
+        if (ADDLN_IN(604, 4 * c * VEC, 4 * VEC, 4 * static_cast<int64_t>(H)))
+          load_gamma<VEC>(p.gamma + c * VEC, gg);
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
           xh[k][i] = (xh[k][i] - mu) * rs;
@@ -196,15 +212,16 @@ __global__ void __launch_bounds__(THREADS) k_bwd_cta(const BwdArgs p) {
         const int c = tid + THREADS * k;
         float d[VEC], gg[VEC], o[VEC], rr[VEC];
         IO::unpack(dv[k], d);
-        load_gamma<VEC>(p.gamma + c * VEC, gg);
-        if (p.dres != nullptr)
+        if (ADDLN_IN(605, 4 * c * VEC, 4 * VEC, 4 * static_cast<int64_t>(H)))
+          load_gamma<VEC>(p.gamma + c * VEC, gg);
+        if (p.dres != nullptr && ADDLN_IN(606, boff + c * 16, 16, bw_rows_bytes(p, S)))
           IO::unpack(ld_stream_v4(static_cast<const char*>(p.dres) + boff + c * 16), rr);
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
           o[i] = rs * (d[i] * gg[i] - fmaf(xh[k][i], mgx, mg));
           if (p.dres != nullptr) o[i] += rr[i];
         }
-        st_stream_v4(drow + c * 16, IO::pack(o));
+        if (ADDLN_IN(607, boff + c * 16, 16, bw_rows_bytes(p, S))) st_stream_v4(drow + c * 16, IO::pack(o));
       }
     }
   }
@@ -216,8 +233,10 @@ __global__ void __launch_bounds__(THREADS) k_bwd_cta(const BwdArgs p) {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
           const int j = (tid + THREADS * k) * VEC + i;
-          out[j] = part[(k * VEC + i) * THREADS + tid];
-          out[H + j] = part[kHalf + (k * VEC + i) * THREADS + tid];
+          if (ADDLN_IN(608, (static_cast<int64_t>(blockIdx.x) * 2 * H + H + j) * 4, 4, bw_ws_bytes(p))) {
+            out[j] = part[(k * VEC + i) * THREADS + tid];
+            out[H + j] = part[kHalf + (k * VEC + i) * THREADS + tid];
+          }
         }
   }
 }
@@ -286,8 +305,10 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
       const int64_t rr = row + s * stride;
       if (rr >= p.rows) break;
       const int64_t off = rr * static_cast<int64_t>(row_bytes) + chunk_off;
-      prefetch_l2(static_cast<const char*>(p.dy) + off, chunk_bytes);
-      prefetch_l2(static_cast<const char*>(p.a) + off, chunk_bytes);
+      if (ADDLN_IN(611, off, chunk_bytes, bw_rows_bytes(p, S))) {
+        prefetch_l2(static_cast<const char*>(p.dy) + off, chunk_bytes);
+        prefetch_l2(static_cast<const char*>(p.a) + off, chunk_bytes);
+      }
     }
   if (tid == 0) {
     for (int i = 0; i < stages * NW; ++i) mbar_init(smem_addr(&bars[i]), 1);
@@ -301,9 +322,10 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
   auto region = [&](int s) { return smem0 + static_cast<uint32_t>(s * NW + warp) * kRegion; };
   auto issue = [&](int s, int64_t rr) {  // lane 0: the warp's chunk of row rr into slot s
     const uint32_t bar = smem_addr(&bars[s * NW + warp]);
-    mbar_arrive_expect_tx(bar, 2u * chunk_bytes);
-    if (chunk_bytes != 0) {
-      const int64_t off = rr * static_cast<int64_t>(row_bytes) + chunk_off;
+    const int64_t off = rr * static_cast<int64_t>(row_bytes) + chunk_off;
+    const bool okc = ADDLN_IN(612, off, chunk_bytes, bw_rows_bytes(p, S));
+    mbar_arrive_expect_tx(bar, okc ? 2u * chunk_bytes : 0u);
+    if (chunk_bytes != 0 && okc) {
       bulk_g2s(region(s), static_cast<const char*>(p.dy) + off, chunk_bytes, bar, policy);
       bulk_g2s(region(s) + CV * 16u, static_cast<const char*>(p.a) + off, chunk_bytes, bar, policy);
     }
@@ -318,7 +340,8 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
 #pragma unroll
     for (int q = 0; q < P / 2; ++q) {
       float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (ok[k]) g = ld_param_f4(p.gamma + (v0 + 32 * k) * VEC + 4 * q);
+      if (ok[k] && ADDLN_IN(613, 4 * ((v0 + 32 * k) * VEC + 4 * q), 16, 4 * static_cast<int64_t>(H)))
+        g = ld_param_f4(p.gamma + (v0 + 32 * k) * VEC + 4 * q);
       gam[k][2 * q] = make_float2(g.x, g.y);
       gam[k][2 * q + 1] = make_float2(g.z, g.w);
     }
@@ -329,14 +352,16 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
   // mean and rstd of the next row are loaded one row ahead, off the row's
   // critical path
   float mu_n = 0.f, rs_n = 0.f;
-  if (row < p.rows) mu_n = __ldg(p.mean + row), rs_n = __ldg(p.rstd + row);
+  if (row < p.rows && ADDLN_IN(602, 4 * row, 4, 4 * p.rows))
+    mu_n = __ldg(p.mean + row), rs_n = __ldg(p.rstd + row);
 
   bool failed = false;
   uint32_t ring = 0;  // ring position of the row: slot, phase, parity
   for (; row < p.rows; row += stride, ring = ring_next(ring, stages)) {
     const int s = static_cast<int>(ring_slot(ring));
     const float mu = mu_n, rs = rs_n;
-    if (row + stride < p.rows) mu_n = __ldg(p.mean + row + stride), rs_n = __ldg(p.rstd + row + stride);
+    if (row + stride < p.rows && ADDLN_IN(603, 4 * (row + stride), 4, 4 * p.rows))
+      mu_n = __ldg(p.mean + row + stride), rs_n = __ldg(p.rstd + row + stride);
     // warp-uniform: every lane polls the warp's barrier with its own clock
     const bool timed_out = __any_sync(
         0xffffffffu, !mbar_wait_bounded(smem_addr(&bars[s * NW + warp]),
@@ -446,7 +471,8 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
             g[q] = mul2(d[q], gam[k][q]);
           }
         }
-        if (p.dres != nullptr)
+        if (p.dres != nullptr &&
+            ADDLN_IN(614, row * static_cast<int64_t>(row_bytes) + c * 16, 16, bw_rows_bytes(p, S)))
           IO::to_pairs(ld_stream_v4(static_cast<const char*>(p.dres) +
                                     row * static_cast<int64_t>(row_bytes) + c * 16),
                        rr);
@@ -455,7 +481,8 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
           o[q] = mul2(rs2, add2(g[q], fma2(x[q], nmgx, nmg)));
           if (p.dres != nullptr) o[q] = add2(o[q], rr[q]);
         }
-        st_stream_v4(drow + static_cast<int64_t>(c) * 16, IO::from_pairs(o));
+        if (ADDLN_IN(615, row * static_cast<int64_t>(row_bytes) + c * 16, 16, bw_rows_bytes(p, S)))
+          st_stream_v4(drow + static_cast<int64_t>(c) * 16, IO::from_pairs(o));
       }
     }
     if constexpr (ROWWARP) {
@@ -489,7 +516,8 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
       float t = part[j];
 #pragma unroll
       for (int w = 1; w < NW; ++w) t += part[static_cast<int64_t>(w) * 2 * H + j];
-      out[j] = t;
+      if (ADDLN_IN(616, (static_cast<int64_t>(blockIdx.x) * 2 * H + j) * 4, 4, bw_ws_bytes(p)))
+        out[j] = t;
     }
   } else {
     float* out = p.ws + static_cast<int64_t>(blockIdx.x) * 2 * H;
@@ -499,6 +527,8 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((bwd_res_regs<DT, THREADS
 #pragma unroll
         for (int q = 0; q < P / 2; ++q) {
           const int j = (v0 + 32 * k) * VEC + 4 * q;
+          if (!ADDLN_IN(617, (static_cast<int64_t>(blockIdx.x) * 2 * H + H + j) * 4, 16, bw_ws_bytes(p)))
+            continue;
           *reinterpret_cast<float4*>(out + j) =
               make_float4(dg[k][2 * q].x, dg[k][2 * q].y, dg[k][2 * q + 1].x, dg[k][2 * q + 1].y);
           *reinterpret_cast<float4*>(out + H + j) =
@@ -527,11 +557,13 @@ __global__ void __launch_bounds__(THREADS) k_bwd_scalar(const BwdArgs p) {
   int64_t it = 0;
   for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
     const int64_t base = row * static_cast<int64_t>(H);
-    const float mu = __ldg(p.mean + row), rs = __ldg(p.rstd + row);
+    float mu = 0.f, rs = 0.f;
+    if (ADDLN_IN(621, 4 * row, 4, 4 * p.rows)) mu = __ldg(p.mean + row), rs = __ldg(p.rstd + row);
     float sg = 0.f, sgx = 0.f;
     for (int j = tid; j < H; j += THREADS) {
-      const float d = IO::load1(p.dy, base + j);
-      const float xh = (IO::load1(p.a, base + j) - mu) * rs;
+      const bool okj = ADDLN_IN(622, (base + j) * IO::kBytes, IO::kBytes, bw_rows_bytes(p, IO::kBytes));
+      const float d = okj ? IO::load1(p.dy, base + j) : 0.f;
+      const float xh = ((okj ? IO::load1(p.a, base + j) : 0.f) - mu) * rs;
       const float g = d * __ldg(p.gamma + j);
       sg_[j] = g;
       sx_[j] = xh;
@@ -555,13 +587,17 @@ __global__ void __launch_bounds__(THREADS) k_bwd_scalar(const BwdArgs p) {
     const float mg = tg * p.inv_h, mgx = tgx * p.inv_h;
     for (int j = tid; j < H; j += THREADS) {
       float o = rs * (sg_[j] - fmaf(sx_[j], mgx, mg));
-      if (p.dres != nullptr) o += IO::load1(p.dres, base + j);
-      IO::store1(p.dx, base + j, o);
+      if (ADDLN_IN(623, (base + j) * IO::kBytes, IO::kBytes, bw_rows_bytes(p, IO::kBytes))) {
+        if (p.dres != nullptr) o += IO::load1(p.dres, base + j);
+        IO::store1(p.dx, base + j, o);
+      }
     }
   }
   if (cols) {
     float* out = p.ws + static_cast<int64_t>(blockIdx.x) * 2 * H;
     for (int j = tid; j < H; j += THREADS) {
+      if (!ADDLN_IN(624, (static_cast<int64_t>(blockIdx.x) * 2 * H + H + j) * 4, 4, bw_ws_bytes(p)))
+        continue;
       out[j] = part[j];
       out[H + j] = part[H + j];
     }
@@ -597,7 +633,7 @@ __global__ void __launch_bounds__(kColCols * SLICES, 32 / SLICES) k_colsum(const
 #pragma unroll
       for (int u = 0; u < kColAcc; ++u) {
         const int64_t bu = b + static_cast<int64_t>(u) * SLICES;
-        if (bu < G) acc[u] += ws[bu * ld + j];
+        if (bu < G && ADDLN_IN(631, (bu * ld + j) * 4, 4, G * ld * 4)) acc[u] += ws[bu * ld + j];
       }
     }
   }
@@ -609,7 +645,7 @@ __global__ void __launch_bounds__(kColCols * SLICES, 32 / SLICES) k_colsum(const
     for (int q = 1; q < SLICES; ++q) t += part[q][lc];
     if (j < H)
       dgamma[j] = t;
-    else
+    else if (ADDLN_IN(632, 4 * (j - H), 4, 4 * static_cast<int64_t>(H)))
       dbeta[j - H] = t;
   }
 }
@@ -845,6 +881,8 @@ int launch_bwd(int dtype, const void* dy, const void* a, const float* mean, cons
   }
   return ADDLN_OK;
 }
+
+ADDLN_BOUNDS_READER(read_bounds_bwd)
 
 int read_and_clear_bwd_error(int* code) {
   int v = 0;

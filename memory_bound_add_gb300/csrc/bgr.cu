@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* 
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int64_t i = w0 + static_cast<int64_t>(u) * kThreads;
-      if (i + 32 <= nvec) {
+      if (i + 32 <= nvec && ADDLN_IN(401, i * 16, 512, nvec * 16)) {
         prefetch_l2(xv + i, 512u);
         if constexpr (HAS_R) prefetch_l2(rv + i, 512u);
       }
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* 
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int64_t i = i0 + static_cast<int64_t>(u) * kThreads;
-      if (i < nvec) {
+      if (i < nvec && ADDLN_IN(402, i * 16, 16, nvec * 16)) {
         xs[u] = ld_stream_v4(xv + i);
         if constexpr (HAS_R) rs[u] = ld_stream_v4(rv + i);
       }
@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* 
           const float* bp = bias + cols[u] * VEC;
 #pragma unroll
           for (int q = 0; q < VEC / 4; ++q) {
-            const float4 t = ld_param_f4(bp + 4 * q);
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ADDLN_IN(403, 4 * (cols[u] * VEC + 4 * q), 16, 4 * hvec * VEC)) t = ld_param_f4(bp + 4 * q);
             b[2 * q] = make_float2(t.x, t.y);
             b[2 * q + 1] = make_float2(t.z, t.w);
           }
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) k_ew_vec(const void* x, const void* 
 #pragma unroll
         for (int q = 0; q < P; ++q)
           f[q] = apply2<KIND>(f[q], HAS_R ? g[q] : dup2(0.f), HAS_B ? b[q] : dup2(0.f));
-        st_stream_v4(yv + i, IO::from_pairs(f));
+        if (ADDLN_IN(404, i * 16, 16, nvec * 16)) st_stream_v4(yv + i, IO::from_pairs(f));
       }
     }
   }
@@ -184,10 +185,12 @@ __global__ void __launch_bounds__(kThreads) k_ew_scalar(const void* x, const voi
   const int64_t smod = KIND != kGelu ? step % H : 0;
   int64_t col = KIND != kGelu ? first % H : 0;
   for (int64_t k = first; k < n; k += step) {
-    const float xv = IO::load1(x, k);
-    const float rv = KIND == kBgr ? IO::load1(r, k) : 0.f;
-    const float bv = KIND != kGelu ? __ldg(bias + col) : 0.f;
-    IO::store1(y, k, apply<KIND>(xv, rv, bv));
+    const bool okk = ADDLN_IN(405, k * IO::kBytes, IO::kBytes, n * IO::kBytes);
+    const bool okb = KIND == kGelu || ADDLN_IN(406, 4 * col, 4, 4 * H);
+    const float xv = okk ? IO::load1(x, k) : 0.f;
+    const float rv = KIND == kBgr && okk ? IO::load1(r, k) : 0.f;
+    const float bv = KIND != kGelu && okb ? __ldg(bias + col) : 0.f;
+    if (okk) IO::store1(y, k, apply<KIND>(xv, rv, bv));
     if (KIND != kGelu) {
       col += smod;
       if (col >= H) col -= H;
@@ -244,6 +247,8 @@ int launch_kind(int dtype, const void* x, const void* r, const float* bias, void
 }
 
 }  // namespace ew
+
+ADDLN_BOUNDS_READER(read_bounds_bgr)
 
 int launch_bias_gelu_residual(int dtype, const void* x, const void* r, const float* bias, void* y,
                               int64_t rows, int64_t H, const LaunchCtx& c) {

@@ -21,6 +21,57 @@
 
 namespace addln {
 
+// ----------------------------------------------------------- checked build
+// Built with -DADDLN_CHECK_BOUNDS, every global access of the kernels is
+// first tested against the extent of the buffer it falls in, taken from the
+// launch's own arguments (rows, H, element size, grid).  An access that would
+// leave its buffer is skipped, and the first one met is recorded in this
+// translation unit's bounds word: bit 63 set, the site number in bits 48..62,
+// the byte offset in bits 0..47.  addln_get_device_error reports it as
+// ADDLN_ERR_BOUNDS.  Skipping rather than trapping keeps the context usable,
+// so one process can run the checked library over many shapes.  In the
+// normal build ADDLN_IN is the constant true and compiles away.
+#ifdef ADDLN_CHECK_BOUNDS
+static __device__ unsigned long long g_bounds_error = 0;
+__device__ __forceinline__ bool in_bounds(int site, int64_t off, int64_t len, int64_t extent) {
+  // an access of no bytes touches nothing (e.g. a warp past a short row's
+  // last vector, whose copy is never issued)
+  if (len == 0 || (off >= 0 && len > 0 && off + len <= extent)) return true;
+  atomicCAS(&g_bounds_error, 0ull,
+            (1ull << 63) | (static_cast<unsigned long long>(site & 0x7fff) << 48) |
+                (static_cast<unsigned long long>(off) & 0xffffffffffffull));
+  return false;
+}
+#define ADDLN_IN(site, off, len, extent) \
+  ::addln::in_bounds((site), static_cast<int64_t>(off), static_cast<int64_t>(len), \
+                     static_cast<int64_t>(extent))
+// Host: reads and clears this translation unit's bounds word.
+#define ADDLN_BOUNDS_READER(fn)                                                              \
+  int fn(unsigned long long* out) {                                                          \
+    unsigned long long v = 0, zero = 0;                                                      \
+    if (cudaMemcpyFromSymbol(&v, ::addln::g_bounds_error, sizeof(v)) != cudaSuccess ||       \
+        cudaMemcpyToSymbol(::addln::g_bounds_error, &zero, sizeof(zero)) != cudaSuccess)     \
+      return ADDLN_ERR_CUDA;                                                                 \
+    *out = v;                                                                                \
+    return ADDLN_OK;                                                                         \
+  }
+#else
+#define ADDLN_IN(site, off, len, extent) true
+#define ADDLN_BOUNDS_READER(fn)    \
+  int fn(unsigned long long* out) { \
+    *out = 0;                       \
+    return ADDLN_OK;                \
+  }
+#endif
+
+// Byte extents of a row launch's buffers (for ADDLN_IN): a [rows, H] tensor
+// in the I/O dtype, a per-column fp32 [H] vector, a per-row fp32 [rows] one.
+__device__ __forceinline__ int64_t rows_bytes(const RowArgs& p, int elem) {
+  return p.rows * static_cast<int64_t>(p.H) * elem;
+}
+__device__ __forceinline__ int64_t cols_bytes(const RowArgs& p) { return 4 * static_cast<int64_t>(p.H); }
+__device__ __forceinline__ int64_t stat_bytes(const RowArgs& p) { return 4 * p.rows; }
+
 // ------------------------------------------------------------ fp32 pairs
 // sm_100 and later execute an fp32 add, multiply or fma on a pair of values
 // as one instruction.  The vector paths of the row kernels keep their fp32

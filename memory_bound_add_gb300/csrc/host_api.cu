@@ -144,6 +144,7 @@ __global__ void k_params_in(const float* g, const float* b, float* gd, float* bd
   addln::pdl_wait();
   const int step = gridDim.x * blockDim.x;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < H; i += step) {
+    if (!ADDLN_IN(701, 4 * i, 4, 4 * static_cast<int64_t>(H))) continue;
     gd[i] = g[i];
     bd[i] = b[i];
   }
@@ -178,6 +179,10 @@ int pipe_of_current_device(Pipe** out) {
 }
 
 }  // namespace
+
+namespace addln {
+ADDLN_BOUNDS_READER(read_bounds_host)
+}  // namespace addln
 
 extern "C" int64_t add_layernorm_fwd_host_workspace_size(int64_t rows, int64_t H, int dtype,
                                                         int want_resid, int want_stats) {

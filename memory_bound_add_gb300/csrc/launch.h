@@ -104,6 +104,17 @@ void note_cuda_error(int err);
 // Device error word (set by a kernel whose bounded wait ran out).
 int read_and_clear_device_error(void* stream, int* code);
 
+// Checked build (-DADDLN_CHECK_BOUNDS): each translation unit's bounds word,
+// read and cleared (0: no access was out of bounds; always 0 in the normal
+// build, which has no word and makes no CUDA call here).
+int read_bounds_rows_warp(unsigned long long* word);
+int read_bounds_rows_cta(unsigned long long* word);
+int read_bounds_softmax(unsigned long long* word);
+int read_bounds_bgr(unsigned long long* word);
+int read_bounds_add(unsigned long long* word);
+int read_bounds_bwd(unsigned long long* word);
+int read_bounds_host(unsigned long long* word);
+
 // Largest H per dtype (shared memory and register budget of the CTA paths).
 constexpr int64_t kMaxHidden16 = 32768;
 constexpr int64_t kMaxHidden32 = 16384;

@@ -147,8 +147,10 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
         const int64_t rr = row + s * stride;
         if (rr >= p.rows) break;
         const int64_t off = rr * static_cast<int64_t>(row_bytes) + chunk_off;
-        prefetch_l2(static_cast<const char*>(p.x) + off, chunk_bytes);
-        if (has_r) prefetch_l2(static_cast<const char*>(p.r) + off, chunk_bytes);
+        if (ADDLN_IN(201, off, chunk_bytes, rows_bytes(p, S)))
+          prefetch_l2(static_cast<const char*>(p.x) + off, chunk_bytes);
+        if (has_r && ADDLN_IN(202, off, chunk_bytes, rows_bytes(p, S)))
+          prefetch_l2(static_cast<const char*>(p.r) + off, chunk_bytes);
       }
     if (tid == 0) {
       for (int s = 0; s < stages * NW; ++s) mbar_init(smem_addr(&bars[s]), 1);
@@ -163,12 +165,16 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
   // Lane 0 of each warp: stage the warp's chunk of row `rr` into slot `s`.
   auto issue = [&](int s, int64_t rr) {
     const uint32_t bar = smem_addr(&bars[s * NW + warp]);
-    mbar_arrive_expect_tx(bar, has_r ? 2u * chunk_bytes : chunk_bytes);
+    const int64_t off = rr * static_cast<int64_t>(row_bytes) + chunk_off;
+    // checked build: a copy that would leave its buffer is not issued, and
+    // the barrier is not told to expect its bytes either
+    const bool okx = ADDLN_IN(203, off, chunk_bytes, rows_bytes(p, S));
+    const bool okr = has_r && ADDLN_IN(204, off, chunk_bytes, rows_bytes(p, S));
+    mbar_arrive_expect_tx(bar, (okx ? chunk_bytes : 0u) + (okr ? chunk_bytes : 0u));
     if (chunk_bytes != 0) {
-      const int64_t off = rr * static_cast<int64_t>(row_bytes) + chunk_off;
       const uint32_t dst = smem0 + s * slot + chunk_off;
-      bulk_g2s(dst, static_cast<const char*>(p.x) + off, chunk_bytes, bar, policy);
-      if (has_r) bulk_g2s(dst + rb, static_cast<const char*>(p.r) + off, chunk_bytes, bar, policy);
+      if (okx) bulk_g2s(dst, static_cast<const char*>(p.x) + off, chunk_bytes, bar, policy);
+      if (okr) bulk_g2s(dst + rb, static_cast<const char*>(p.r) + off, chunk_bytes, bar, policy);
     }
   };
   if constexpr (TMA) {
@@ -185,8 +191,8 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
 #pragma unroll
       for (int q = 0; q < P / 2; ++q) {
         float4 g = make_float4(0.f, 0.f, 0.f, 0.f), b = g;
-        if (ok[k]) {
-          const int c = v0 + 32 * k;
+        const int c = v0 + 32 * k;
+        if (ok[k] && ADDLN_IN(205, 4 * (c * VEC + 4 * q), 16, cols_bytes(p))) {
           g = ld_param_f4(p.gamma + c * VEC + 4 * q);
           b = ld_param_f4(p.beta + c * VEC + 4 * q);
         }
@@ -233,12 +239,14 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
       uint4 xv[NV], rv[NV];
 #pragma unroll
       for (int k = 0; k < NV; ++k)
-        if (ok[k]) xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(v0 + 32 * k) * 16);
+        if (ok[k] && ADDLN_IN(206, base * S + (v0 + 32 * k) * 16, 16, rows_bytes(p, S)))
+          xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(v0 + 32 * k) * 16);
       if (has_r) {
         const char* rrow = static_cast<const char*>(p.r) + base * S;
 #pragma unroll
         for (int k = 0; k < NV; ++k)
-          if (ok[k]) rv[k] = ld_stream_v4(rrow + static_cast<int64_t>(v0 + 32 * k) * 16);
+          if (ok[k] && ADDLN_IN(207, base * S + (v0 + 32 * k) * 16, 16, rows_bytes(p, S)))
+            rv[k] = ld_stream_v4(rrow + static_cast<int64_t>(v0 + 32 * k) * 16);
 #pragma unroll
         for (int k = 0; k < NV; ++k)
           if (ok[k]) IO::sum_pairs(xv[k], rv[k], v[k]);
@@ -256,7 +264,7 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
       char* arow = static_cast<char*>(p.a) + base * S;
 #pragma unroll
       for (int k = 0; k < NV; ++k)
-        if (ok[k])
+        if (ok[k] && ADDLN_IN(208, base * S + (v0 + 32 * k) * 16, 16, rows_bytes(p, S)))
           st_stream_v4(arow + static_cast<int64_t>(v0 + 32 * k) * 16, IO::from_pairs(v[k]));
     }
 
@@ -314,18 +322,22 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
         } else {
 #pragma unroll
           for (int qq = 0; qq < P / 2; ++qq) {
-            const float4 g = ld_param_f4(p.gamma + c * VEC + 4 * qq);
-            const float4 b = ld_param_f4(p.beta + c * VEC + 4 * qq);
+            float4 g = make_float4(0.f, 0.f, 0.f, 0.f), b = g;
+            if (ADDLN_IN(209, 4 * (c * VEC + 4 * qq), 16, cols_bytes(p))) {
+              g = ld_param_f4(p.gamma + c * VEC + 4 * qq);
+              b = ld_param_f4(p.beta + c * VEC + 4 * qq);
+            }
             o[2 * qq] =
                 normalise2(v[k][2 * qq], negm, rstd2, make_float2(g.x, g.y), make_float2(b.x, b.y));
             o[2 * qq + 1] =
                 normalise2(v[k][2 * qq + 1], negm, rstd2, make_float2(g.z, g.w), make_float2(b.z, b.w));
           }
         }
-        st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::from_pairs(o));
+        if (ADDLN_IN(210, base * S + c * 16, 16, rows_bytes(p, S)))
+          st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::from_pairs(o));
       }
     }
-    if (tid == 0) {
+    if (tid == 0 && ADDLN_IN(211, 4 * row, 4, stat_bytes(p))) {
       if (p.mean != nullptr) p.mean[row] = K0 + tot.m;
       if (p.rstd != nullptr) p.rstd[row] = rstd;
     }
@@ -353,13 +365,19 @@ __global__ void __launch_bounds__(THREADS) k_cta_scalar(const RowArgs p) {
   int64_t it = 0;
   for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
     const int64_t base = row * static_cast<int64_t>(H);
-    const float K = has_r ? IO::load1(p.x, base) + IO::load1(p.r, base) : IO::load1(p.x, base);
+    constexpr int S = IO::kBytes;
+    float K = 0.f;
+    if (ADDLN_IN(221, base * S, S, rows_bytes(p, S)))
+      K = has_r ? IO::load1(p.x, base) + IO::load1(p.r, base) : IO::load1(p.x, base);
     float sum = 0.f;
     int cnt = 0;
 #pragma unroll 8
     for (int j = tid; j < H; j += THREADS) {
-      float a = IO::load1(p.x, base + j);
-      if (has_r) a += IO::load1(p.r, base + j);
+      float a = 0.f;
+      if (ADDLN_IN(222, (base + j) * S, S, rows_bytes(p, S))) {
+        a = IO::load1(p.x, base + j);
+        if (has_r) a += IO::load1(p.r, base + j);
+      }
       sa[j] = a;
       sum += a - K;
       ++cnt;
@@ -382,10 +400,12 @@ __global__ void __launch_bounds__(THREADS) k_cta_scalar(const RowArgs p) {
 #pragma unroll 4
     for (int j = tid; j < H; j += THREADS) {
       const float a = sa[j];
-      IO::store1(p.y, base + j, normalise(a, K, tot.m, rstd, __ldg(p.gamma + j), __ldg(p.beta + j)));
-      if (p.a != nullptr) IO::store1(p.a, base + j, a);
+      if (ADDLN_IN(223, 4 * j, 4, cols_bytes(p)) && ADDLN_IN(224, (base + j) * S, S, rows_bytes(p, S))) {
+        IO::store1(p.y, base + j, normalise(a, K, tot.m, rstd, __ldg(p.gamma + j), __ldg(p.beta + j)));
+        if (p.a != nullptr) IO::store1(p.a, base + j, a);
+      }
     }
-    if (tid == 0) {
+    if (tid == 0 && ADDLN_IN(225, 4 * row, 4, stat_bytes(p))) {
       if (p.mean != nullptr) p.mean[row] = K + tot.m;
       if (p.rstd != nullptr) p.rstd[row] = rstd;
     }
@@ -573,6 +593,8 @@ int launch_cta_scalar(int dtype, const RowArgs& p, const LaunchCtx& c, const cha
     default: return ADDLN_ERR_DTYPE;
   }
 }
+
+ADDLN_BOUNDS_READER(read_bounds_rows_cta)
 
 int read_and_clear_device_error(void* stream, int* code) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ADDLN_ERR_CUDA;

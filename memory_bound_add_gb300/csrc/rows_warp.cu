@@ -44,8 +44,10 @@ __global__ void __launch_bounds__(kWarpCtaThreads) __maxnreg__((warp_row_max_reg
   const int64_t base = row * static_cast<int64_t>(H);  // element offset of the row
   if (lane == 0 && row < p.rows) {
     const uint32_t bytes = static_cast<uint32_t>(H) * S;  // whole 16-byte vectors
-    prefetch_l2(static_cast<const char*>(p.x) + base * S, bytes);
-    if (p.r != nullptr) prefetch_l2(static_cast<const char*>(p.r) + base * S, bytes);
+    if (ADDLN_IN(101, base * S, bytes, rows_bytes(p, S)))
+      prefetch_l2(static_cast<const char*>(p.x) + base * S, bytes);
+    if (p.r != nullptr && ADDLN_IN(102, base * S, bytes, rows_bytes(p, S)))
+      prefetch_l2(static_cast<const char*>(p.r) + base * S, bytes);
   }
   pdl_trigger();
   pdl_wait();
@@ -67,13 +69,15 @@ __global__ void __launch_bounds__(kWarpCtaThreads) __maxnreg__((warp_row_max_reg
   uint4 xv[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k)
-    if (ok[k]) xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(lane + 32 * k) * 16);
+    if (ok[k] && ADDLN_IN(103, base * S + (lane + 32 * k) * 16, 16, rows_bytes(p, S)))
+      xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(lane + 32 * k) * 16);
   if (p.r != nullptr) {
     const char* rrow = static_cast<const char*>(p.r) + base * S;
     uint4 rv[NV];
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (ok[k]) rv[k] = ld_stream_v4(rrow + static_cast<int64_t>(lane + 32 * k) * 16);
+      if (ok[k] && ADDLN_IN(104, base * S + (lane + 32 * k) * 16, 16, rows_bytes(p, S)))
+        rv[k] = ld_stream_v4(rrow + static_cast<int64_t>(lane + 32 * k) * 16);
 #pragma unroll
     for (int k = 0; k < NV; ++k)
       if (ok[k]) IO::sum_pairs(xv[k], rv[k], v[k]);
@@ -88,7 +92,8 @@ __global__ void __launch_bounds__(kWarpCtaThreads) __maxnreg__((warp_row_max_reg
     char* arow = static_cast<char*>(p.a) + base * S;
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (ok[k]) st_stream_v4(arow + static_cast<int64_t>(lane + 32 * k) * 16, IO::from_pairs(v[k]));
+      if (ok[k] && ADDLN_IN(105, base * S + (lane + 32 * k) * 16, 16, rows_bytes(p, S)))
+        st_stream_v4(arow + static_cast<int64_t>(lane + 32 * k) * 16, IO::from_pairs(v[k]));
   }
 
   // ---- row statistics on the shifted row: per-lane two-pass, warp butterfly
@@ -112,16 +117,20 @@ __global__ void __launch_bounds__(kWarpCtaThreads) __maxnreg__((warp_row_max_reg
       float2 o[P];
 #pragma unroll
       for (int q = 0; q < P / 2; ++q) {
-        const float4 g = ld_param_f4(p.gamma + c * VEC + 4 * q);
-        const float4 b = ld_param_f4(p.beta + c * VEC + 4 * q);
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), b = g;
+        if (ADDLN_IN(106, 4 * (c * VEC + 4 * q), 16, cols_bytes(p))) {
+          g = ld_param_f4(p.gamma + c * VEC + 4 * q);
+          b = ld_param_f4(p.beta + c * VEC + 4 * q);
+        }
         o[2 * q] = normalise2(v[k][2 * q], negm, rstd2, make_float2(g.x, g.y), make_float2(b.x, b.y));
         o[2 * q + 1] =
             normalise2(v[k][2 * q + 1], negm, rstd2, make_float2(g.z, g.w), make_float2(b.z, b.w));
       }
-      st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::from_pairs(o));
+      if (ADDLN_IN(107, base * S + c * 16, 16, rows_bytes(p, S)))
+        st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::from_pairs(o));
     }
   }
-  if (lane == 0) {
+  if (lane == 0 && ADDLN_IN(108, 4 * row, 4, stat_bytes(p))) {
     if (p.mean != nullptr) p.mean[row] = K + st.m;
     if (p.rstd != nullptr) p.rstd[row] = rstd;
   }
@@ -152,11 +161,13 @@ __global__ void __launch_bounds__(kWarpCtaThreads, 2) k_warp_row(const RowArgs p
   float t[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k)
-    if (ok[k]) v[k][0] = IO::load1(p.x, base + lane + 32 * k);
+    if (ok[k] && ADDLN_IN(111, (base + lane + 32 * k) * IO::kBytes, IO::kBytes, rows_bytes(p, IO::kBytes)))
+      v[k][0] = IO::load1(p.x, base + lane + 32 * k);
   if (p.r != nullptr) {
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (ok[k]) t[k] = IO::load1(p.r, base + lane + 32 * k);
+      if (ok[k] && ADDLN_IN(112, (base + lane + 32 * k) * IO::kBytes, IO::kBytes, rows_bytes(p, IO::kBytes)))
+        t[k] = IO::load1(p.r, base + lane + 32 * k);
 #pragma unroll
     for (int k = 0; k < NV; ++k)
       if (ok[k]) v[k][0] += t[k];
@@ -166,7 +177,8 @@ __global__ void __launch_bounds__(kWarpCtaThreads, 2) k_warp_row(const RowArgs p
   if (p.a != nullptr) {
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (ok[k]) IO::store1(p.a, base + lane + 32 * k, v[k][0]);
+      if (ok[k] && ADDLN_IN(113, (base + lane + 32 * k) * IO::kBytes, IO::kBytes, rows_bytes(p, IO::kBytes)))
+        IO::store1(p.a, base + lane + 32 * k, v[k][0]);
   }
 
   // ---- row statistics on the shifted row: per-lane two-pass, warp butterfly
@@ -183,11 +195,13 @@ __global__ void __launch_bounds__(kWarpCtaThreads, 2) k_warp_row(const RowArgs p
   for (int k = 0; k < NV; ++k) {
     if (ok[k]) {
       const int j = lane + 32 * k;
-      const float g = __ldg(p.gamma + j), b = __ldg(p.beta + j);
-      IO::store1(p.y, base + j, normalise(v[k][0], 0.f, m, rstd, g, b));
+      float g = 0.f, b = 0.f;
+      if (ADDLN_IN(114, 4 * j, 4, cols_bytes(p))) g = __ldg(p.gamma + j), b = __ldg(p.beta + j);
+      if (ADDLN_IN(115, (base + j) * IO::kBytes, IO::kBytes, rows_bytes(p, IO::kBytes)))
+        IO::store1(p.y, base + j, normalise(v[k][0], 0.f, m, rstd, g, b));
     }
   }
-  if (lane == 0) {
+  if (lane == 0 && ADDLN_IN(116, 4 * row, 4, stat_bytes(p))) {
     if (p.mean != nullptr) p.mean[row] = K + m;
     if (p.rstd != nullptr) p.rstd[row] = rstd;
   }
@@ -238,6 +252,8 @@ static int launch_scalar(const RowArgs& p, const LaunchCtx& c, const char** name
   if (nv <= 32) { *name = "warp_scalar_nv32"; return launch<DT, 32, false>(p, c); }
   return ADDLN_ERR_UNSUPPORTED;
 }
+
+ADDLN_BOUNDS_READER(read_bounds_rows_warp)
 
 int launch_warp_row(int dtype, bool vec, const RowArgs& p, const LaunchCtx& c,
                     const char** name) {

@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(kWarpCtaThreads, 2) k_softmax_warp(const RowAr
     uint4 xv[NV];
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (ok[k]) xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(lane + 32 * k) * 16);
+      if (ok[k] && ADDLN_IN(301, base * S + (lane + 32 * k) * 16, 16, rows_bytes(p, S)))
+        xv[k] = ld_stream_v4(xrow + static_cast<int64_t>(lane + 32 * k) * 16);
     float mx = -INFINITY;
 #pragma unroll
     for (int k = 0; k < NV; ++k)
@@ -208,19 +209,24 @@ __global__ void __launch_bounds__(kWarpCtaThreads, 2) k_softmax_warp(const RowAr
       if (ok[k]) {
 #pragma unroll
         for (int q = 0; q < P; ++q) e[k][q] = mul2(e[k][q], inv);
-        st_stream_v4(yrow + static_cast<int64_t>(lane + 32 * k) * 16, IO::from_pairs(e[k]));
+        if (ADDLN_IN(302, base * S + (lane + 32 * k) * 16, 16, rows_bytes(p, S)))
+          st_stream_v4(yrow + static_cast<int64_t>(lane + 32 * k) * 16, IO::from_pairs(e[k]));
       }
     }
   } else {
     float v[NV][1];
 #pragma unroll
-    for (int k = 0; k < NV; ++k) v[k][0] = ok[k] ? IO::load1(p.x, base + lane + 32 * k) : 0.f;
+    for (int k = 0; k < NV; ++k)
+      v[k][0] = ok[k] && ADDLN_IN(303, (base + lane + 32 * k) * S, S, rows_bytes(p, S))
+                    ? IO::load1(p.x, base + lane + 32 * k)
+                    : 0.f;
     const SPart mine = thread_part<NV, 1, FULL>(v, ok);
     const SPart tot = butterfly<32>(mine);
     const float f = rescale(mine.m, tot.m) / tot.s;
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (ok[k]) IO::store1(p.y, base + lane + 32 * k, v[k][0] * f);
+      if (ok[k] && ADDLN_IN(304, (base + lane + 32 * k) * S, S, rows_bytes(p, S)))
+        IO::store1(p.y, base + lane + 32 * k, v[k][0] * f);
   }
 }
 
@@ -266,9 +272,12 @@ __global__ void __launch_bounds__(THREADS) k_softmax_cta(const RowArgs p) {
   const int64_t stride = gridDim.x;
   int64_t row = blockIdx.x;
   auto issue = [&](int64_t rr) {
-    mbar_arrive_expect_tx(bar_a, row_bytes);
-    bulk_g2s(xs, static_cast<const char*>(p.x) + rr * static_cast<int64_t>(row_bytes), row_bytes,
-             bar_a, policy);
+    // checked build: a copy that would leave X is not issued (nor expected)
+    const bool okx = ADDLN_IN(305, rr * static_cast<int64_t>(row_bytes), row_bytes, rows_bytes(p, S));
+    mbar_arrive_expect_tx(bar_a, okx ? row_bytes : 0u);
+    if (okx)
+      bulk_g2s(xs, static_cast<const char*>(p.x) + rr * static_cast<int64_t>(row_bytes), row_bytes,
+               bar_a, policy);
   };
   if (tid == 0 && row < p.rows) issue(row);
 
@@ -327,7 +336,9 @@ __global__ void __launch_bounds__(THREADS) k_softmax_cta(const RowArgs p) {
       if (ok[k]) {
 #pragma unroll
         for (int q = 0; q < P; ++q) e[k][q] = mul2(e[k][q], inv);
-        st_stream_v4(yrow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::from_pairs(e[k]));
+        if (ADDLN_IN(306, row * static_cast<int64_t>(row_bytes) + (tid + THREADS * k) * 16, 16,
+                     rows_bytes(p, S)))
+          st_stream_v4(yrow + static_cast<int64_t>(tid + THREADS * k) * 16, IO::from_pairs(e[k]));
       }
     }
   }
@@ -382,11 +393,11 @@ __global__ void __launch_bounds__(THREADS) k_softmax_cta_smem(const RowArgs p) {
   const int64_t stride = gridDim.x;
   int64_t row = blockIdx.x;
   auto issue = [&](int64_t rr) {  // lane 0: the warp's chunk of row rr
-    mbar_arrive_expect_tx(bar_w, chunk_bytes);
-    if (chunk_bytes != 0)
-      bulk_g2s(xs + chunk_off,
-               static_cast<const char*>(p.x) + rr * static_cast<int64_t>(row_bytes) + chunk_off,
-               chunk_bytes, bar_w, policy);
+    const int64_t off = rr * static_cast<int64_t>(row_bytes) + chunk_off;
+    const bool okx = ADDLN_IN(307, off, chunk_bytes, rows_bytes(p, S));
+    mbar_arrive_expect_tx(bar_w, okx ? chunk_bytes : 0u);
+    if (chunk_bytes != 0 && okx)
+      bulk_g2s(xs + chunk_off, static_cast<const char*>(p.x) + off, chunk_bytes, bar_w, policy);
   };
   if (lane == 0 && row < p.rows) issue(row);
 
@@ -435,7 +446,8 @@ __global__ void __launch_bounds__(THREADS) k_softmax_cta_smem(const RowArgs p) {
       IO::to_pairs(ld_shared_v4(xs + c * 16), v);
 #pragma unroll
       for (int q = 0; q < P; ++q) v[q] = mul2(exp_pair(v[q], negm, log2e), inv);
-      st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::from_pairs(v));
+      if (ADDLN_IN(308, row * static_cast<int64_t>(row_bytes) + c * 16, 16, rows_bytes(p, S)))
+        st_stream_v4(yrow + static_cast<int64_t>(c) * 16, IO::from_pairs(v));
     }
     // every lane of the warp is done with its chunk before it is refilled
     __syncwarp();
@@ -464,7 +476,9 @@ __global__ void __launch_bounds__(THREADS) k_softmax_scalar(const RowArgs p) {
     float mx = -INFINITY;
 #pragma unroll 8
     for (int j = tid; j < H; j += THREADS) {
-      const float a = IO::load1(p.x, base + j);
+      const float a = ADDLN_IN(309, (base + j) * IO::kBytes, IO::kBytes, rows_bytes(p, IO::kBytes))
+                          ? IO::load1(p.x, base + j)
+                          : 0.f;
       se[j] = a;
       mx = fmaxf(mx, a);
     }
@@ -483,7 +497,9 @@ __global__ void __launch_bounds__(THREADS) k_softmax_scalar(const RowArgs p) {
     const SPart tot = butterfly<NW>(rbuf[lane % NW]);
     const float f = rescale(mine.m, tot.m) / tot.s;
 #pragma unroll 4
-    for (int j = tid; j < H; j += THREADS) IO::store1(p.y, base + j, se[j] * f);
+    for (int j = tid; j < H; j += THREADS)
+      if (ADDLN_IN(310, (base + j) * IO::kBytes, IO::kBytes, rows_bytes(p, IO::kBytes)))
+        IO::store1(p.y, base + j, se[j] * f);
   }
 }
 
@@ -670,6 +686,8 @@ int launch_softmax_scalar(int dtype, const RowArgs& p, const LaunchCtx& c, const
     default: return ADDLN_ERR_DTYPE;
   }
 }
+
+ADDLN_BOUNDS_READER(read_bounds_softmax)
 
 int read_and_clear_softmax_error(int* code) {
   int v = 0;

@@ -49,7 +49,7 @@ def test_header_declares_the_expected_entry_points():
         "bias_add_fwd", "gelu_fwd", "add_layernorm_bwd", "add_layernorm_bwd_workspace_size",
         "add_layernorm_bwd_noalloc",
         "addln_strerror",
-        "addln_max_hidden",
+        "addln_max_hidden", "addln_bounds_checked", "addln_bounds_violation",
         "addln_get_device_error", "addln_set_force_path", "addln_set_wait_limit_ns",
         "addln_set_grid_cap", "addln_set_pdl", "addln_set_cta_shape", "addln_last_path",
         "addln_last_cuda_error"])
@@ -72,7 +72,7 @@ def test_binding_signatures_cover_the_header():
     assert (binding.FP32, binding.FP16, binding.BF16) == (d["ADDLN_FP32"], d["ADDLN_FP16"],
                                                           d["ADDLN_BF16"])
     for k in ("NULL", "SHAPE", "DTYPE", "EPS", "ALIAS", "LAUNCH", "UNSUPPORTED",
-              "DEVICE_TIMEOUT", "CUDA", "WORKSPACE"):
+              "DEVICE_TIMEOUT", "CUDA", "WORKSPACE", "BOUNDS"):
         assert getattr(binding, "ERR_" + k) == d["ADDLN_ERR_" + k]
     for k in ("AUTO", "WARP_VEC", "CTA_TMA", "CTA_VEC", "SCALAR"):
         assert getattr(binding, "PATH_" + k) == d["ADDLN_PATH_" + k]
@@ -350,3 +350,17 @@ def test_tolerance_helper_ulp():
     assert y_violations(np.array([1.0 + 5e-3]), np.array([1.0]), "fp16").any()
     assert not y_violations(np.array([1.0 + 1e-5]), np.array([1.0]), "fp32").any()
     assert y_violations(np.array([1.0 + 3e-5]), np.array([1.0]), "fp32").any()
+
+
+def test_bounds_checked_build_loads_and_says_so():
+    # the debugging build compiles every kernel with the bounds tests in, and
+    # loads and answers on a machine without a GPU like the normal build
+    from memory_bound_add_gb300 import binding
+    from memory_bound_add_gb300.build import CHECKED_LIB, build
+    path = build(checked=True)
+    assert path == CHECKED_LIB
+    checked = binding.load(CHECKED_LIB)
+    assert checked.addln_bounds_checked() == 1
+    assert binding.lib().addln_bounds_checked() == 0
+    assert checked.addln_bounds_violation() == 0
+    assert checked.addln_strerror(binding.ERR_BOUNDS).decode().startswith("a kernel skipped")

@@ -69,8 +69,8 @@ def test_committed_record_names_the_bench_default_kernel():
 
 
 def test_buffer_sets_continue_the_rotation_across_replays():
-    # the set count divides K when it can, so replay r + 1 picks up the
-    # rotation where replay r left it
+    # the set count divides the steps a replay launches when it can, so
+    # replay r + 1 picks up the rotation where replay r left it
     assert bench.pick_sets(20, 9, 50, 10 ** 9) == (10, False)
     assert bench.pick_sets(20, 2, 2 * 10 ** 9, 10 ** 11) == (2, False)
     assert bench.pick_sets(23, 9, 50, 10 ** 9) == (23, False)
