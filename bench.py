@@ -80,6 +80,8 @@ def parse_args():
     ap.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch (1/0)")
     ap.add_argument("--cta-threads", type=int, default=0, help="TMA kernel threads per CTA (tuning)")
     ap.add_argument("--stages", type=int, default=0, help="TMA kernel staged rows per CTA (tuning)")
+    ap.add_argument("--warp-rows", type=int, default=0,
+                    help="rows a warp takes on the warp-per-row vector path (0 = by shape; tuning)")
     ap.add_argument("--backward", action="store_true",
                     help="time add_layernorm_bwd on an Add+LayerNorm workload")
     ap.add_argument("--chain", type=int, default=0,
@@ -503,6 +505,9 @@ def config_summary(w, m, peak):
         tu = m["unfused"]["median_s"] / m["steps"]
         out["unfused_us_per_step"] = round(tu * 1e6, 3)
         out["fused_speedup"] = round(tu / t, 3)
+    tr = profiled_traffic(w.name, m["path"])
+    out["traffic"] = tr["bytes"] if tr else None
+    out["traffic_over_algorithmic"] = round(tr["bytes"] / alg, 4) if tr else None
     return out
 
 
@@ -535,6 +540,7 @@ def run_ours(args):
     mba.addln_set_grid_cap(args.grid_cap)
     mba.addln_set_pdl(args.pdl)
     mba.addln_set_cta_shape(args.cta_threads, args.stages)
+    mba.addln_set_warp_rows(args.warp_rows)
 
     sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
     if sampler:
@@ -664,6 +670,7 @@ def run_ours(args):
     mba.addln_set_force_path(0)
     mba.addln_set_grid_cap(0)
     mba.addln_set_cta_shape(0, 0)
+    mba.addln_set_warp_rows(0)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws > 1:
@@ -1044,6 +1051,9 @@ def run_backward(args):
     need = max(2, math.ceil(3 * l2 / per_set))
     n_sets, needs_flush = pick_sets(replay_lead(K) + K, need, per_set, device_budget(dev))
     wsb = mba.add_layernorm_bwd_workspace_size(w.rows, w.H, mba.binding.DTYPE_CODE[d["x"].dtype])
+    # one workspace reused by every step, as a training loop reuses its
+    # scratch (the inputs and outputs rotate over the sets)
+    ws_shared = mba.bwd_workspace(w.rows, w.H, d["x"].dtype, dev)
     sets = []
     x, r = d["x"].to(dev), d["r"].to(dev)
     for i in range(n_sets):
@@ -1054,7 +1064,7 @@ def run_backward(args):
         sets.append({"dy": synth.make_grad(w, seed=args.seed + i).to(dev), "a": a, "mean": mean,
                      "rstd": rstd, "dx": torch.empty_like(x),
                      "dg": torch.empty(w.H, device=dev), "db": torch.empty(w.H, device=dev),
-                     "ws": torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)})
+                     "ws": ws_shared})
     torch.cuda.synchronize()
 
     def step(i):
@@ -1084,6 +1094,7 @@ def run_backward(args):
         "config": {"workload": w.name, "rows": w.rows, "H": w.H, "io_dtype": w.dtype,
                    "outputs": "dX, dgamma, dbeta", "kernel_path": path,
                    "algorithmic_bytes_per_step": alg, "workspace_bytes": wsb,
+                   "workspace": "one workspace reused by every step",
                    "l2": f"inputs rotate over {n_sets} buffer sets (>= 3x L2)"
                          + ("; L2 flushed between replays" if needs_flush else ""),
                    "timing": (f"one CUDA graph of {run['lead']} untimed and K={K} timed steps "

@@ -225,7 +225,9 @@ int gelu_fwd(const void *t, void *u, int64_t n, int dtype, void *stream);
  *   workspace  device scratch of at least add_layernorm_bwd_workspace_size()
  *              bytes, 16-byte aligned, owned by the caller; needed only with
  *              dgamma / dbeta.  Holds per-CTA column partials, summed in a
- *              fixed order, so the results are bitwise reproducible.
+ *              fixed order, so the results are bitwise reproducible.  Its
+ *              contents need no initialisation; calls that may overlap on
+ *              the GPU must not share a workspace.
  * rows == 0 zero-fills dgamma and dbeta.  fp32 arithmetic; dx rounded to
  * nearest even.  Returns ADDLN_OK, or a negative code (ADDLN_ERR_WORKSPACE
  * for a missing, short or misaligned workspace).
@@ -262,13 +264,14 @@ int64_t add_layernorm_bwd_workspace_size(int64_t rows, int64_t H, int dtype);
  * with that device current, and caches it for the device's current context
  * (after cudaDeviceReset the new context's address is looked up again); make
  * that first call before any stream capture.  Argument errors are reported
- * with the same codes, checked in the same order, as add_layernorm_bwd.  A shape whose partials need
- * more than the buffer (add_layernorm_bwd_workspace_size() >
- * ADDLN_NOALLOC_SCRATCH_BYTES) is rejected with ADDLN_ERR_WORKSPACE before any
- * launch.  All calls on a device share the buffer, which keeps the last call's
- * contents (nothing in it needs to start at zero): calls that may overlap on
- * the GPU, from other streams or host threads, race on it and must be
- * serialised by the caller.
+ * with the same codes, checked in the same order, as add_layernorm_bwd.  A
+ * shape whose workspace would exceed the buffer
+ * (add_layernorm_bwd_workspace_size() > ADDLN_NOALLOC_SCRATCH_BYTES) is
+ * rejected with ADDLN_ERR_WORKSPACE before any launch.  All calls on a
+ * device share the buffer, which keeps the last call's contents (nothing in
+ * it needs to start at zero): calls that may overlap on the GPU, from other
+ * streams or host threads, race on it and must be serialised by the
+ * caller.
  */
 int add_layernorm_bwd_noalloc(const void *dy, const void *a, const float *mean,
                               const float *rstd, const float *gamma, const void *dres, void *dx,
@@ -359,6 +362,16 @@ int addln_set_pdl(int on);
  * ADDLN_ERR_SHAPE for a value out of range.
  */
 int addln_set_cta_shape(int threads, int stages);
+
+/*
+ * Test and benchmark only.  Rows each warp takes on the warp-per-row vector
+ * path of add_layernorm_fwd / layernorm_fwd (rows of up to 1024 elements):
+ * 0 (default) = two for rows of 3 or 4 16-byte vectors a lane when the call
+ * has at least 16 rows per SM, else one; 1 or 2 forces it (rows of other
+ * lengths always take one).  Returns the previous setting, or
+ * ADDLN_ERR_SHAPE for another value.
+ */
+int addln_set_warp_rows(int rows);
 
 /* Name of the kernel path the last add_layernorm_fwd / layernorm_fwd call on
  * this host thread launched (static text; "none" before the first launch). */

@@ -61,6 +61,7 @@ SIGNATURES = {
     "addln_set_grid_cap": (ctypes.c_int64, [ctypes.c_int64]),
     "addln_set_pdl": (ctypes.c_int, [ctypes.c_int]),
     "addln_set_cta_shape": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+    "addln_set_warp_rows": (ctypes.c_int, [ctypes.c_int]),
     "addln_last_path": (ctypes.c_char_p, []),
     "addln_last_cuda_error": (ctypes.c_char_p, []),
 }
@@ -357,12 +358,19 @@ def add_layernorm_bwd_workspace_size(rows: int, H: int, dtype: int) -> int:
     return n
 
 
+def bwd_workspace(rows: int, H: int, dtype, device=None):
+    """A workspace for add_layernorm_bwd on rows x H of dtype (a torch dtype)."""
+    nbytes = add_layernorm_bwd_workspace_size(rows, H, DTYPE_CODE[dtype])
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device or "cuda")
+
+
 def add_layernorm_bwd(dy, a, mean, rstd, gamma, dx, dgamma=None, dbeta=None, dres=None,
                       workspace=None, stream=None):
     """Backward of add_layernorm_fwd into caller-provided dx (and dgamma,
     dbeta).  workspace: a CUDA tensor of at least
-    add_layernorm_bwd_workspace_size(rows, H, dtype) bytes (allocated here
-    with PyTorch when None and dgamma is wanted)."""
+    add_layernorm_bwd_workspace_size(rows, H, dtype) bytes, reusable call
+    after call (bwd_workspace makes one; allocated here when None and dgamma
+    is wanted)."""
     rows, H = _rows_shape(dy)
     _require(dy, "dy")
     for t, n in ((a, "a"), (dx, "dx"), (dres, "dres")):
@@ -370,8 +378,7 @@ def add_layernorm_bwd(dy, a, mean, rstd, gamma, dx, dgamma=None, dbeta=None, dre
             _require(t, n, dy.dtype, like=dy)
     dt = DTYPE_CODE[dy.dtype]
     if dgamma is not None and workspace is None:
-        nbytes = add_layernorm_bwd_workspace_size(rows, H, dt)
-        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dy.device)
+        workspace = bwd_workspace(rows, H, dy.dtype, dy.device)
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().add_layernorm_bwd(_ptr(dy), _ptr(a), _ptr(mean), _ptr(rstd), _ptr(gamma),
                                    _ptr(dres), _ptr(dx), _ptr(dgamma), _ptr(dbeta), rows, H, dt,
@@ -433,6 +440,15 @@ def addln_set_pdl(on: bool) -> int:
 
 def addln_set_cta_shape(threads: int, stages: int) -> int:
     return int(lib().addln_set_cta_shape(int(threads), int(stages)))
+
+
+def addln_set_warp_rows(rows: int) -> int:
+    """Test and benchmark only: rows a warp takes on the warp-per-row vector
+    path (0 = by shape, 1 or 2 forced).  Returns the previous setting."""
+    rc = int(lib().addln_set_warp_rows(int(rows)))
+    if rc < 0:
+        raise AddLNError(rc, "addln_set_warp_rows")
+    return rc
 
 
 def addln_last_path() -> str:

@@ -31,6 +31,7 @@ std::atomic<int64_t> g_grid_cap{0};
 std::atomic<int> g_pdl{1};
 std::atomic<int> g_cta_threads{0};
 std::atomic<int> g_stages{0};
+std::atomic<int> g_warp_rows{0};
 std::atomic<uint64_t> g_bounds_violation{0};
 thread_local const char* g_last_path = "none";
 thread_local int g_last_cuda_error = 0;
@@ -138,6 +139,7 @@ int run_rows(const RowArgs& p, int dtype, void* stream, bool allow_tma = true) {
   c.pdl = g_pdl.load(std::memory_order_relaxed) != 0;
   c.cta_threads = g_cta_threads.load(std::memory_order_relaxed);
   c.stages = g_stages.load(std::memory_order_relaxed);
+  c.warp_rows = g_warp_rows.load(std::memory_order_relaxed);
   const int rc = device_info(&c.dev);
   if (rc != ADDLN_OK) return rc;
 
@@ -486,6 +488,12 @@ int addln_set_cta_shape(int threads, int stages) {
 }
 
 const char* addln_last_path(void) { return g_last_path; }
+
+int addln_set_warp_rows(int rows) {
+  if (rows < 0 || rows > 2) return ADDLN_ERR_SHAPE;
+  return g_warp_rows.exchange(rows);
+}
+
 
 const char* addln_last_cuda_error(void) {
   return g_last_cuda_error == 0 ? "none"

@@ -675,10 +675,15 @@ int resident(const void* f, int threads, int smem, const DeviceInfo& dev) {
     if (it != g_occ.end()) return it->second;
   }
   // per-function limit: raised once to the opt-in maximum, never lowered
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin) !=
-          cudaSuccess)
-    return -1;
+  // Raised to the device's opt-in maximum less the kernel's static shared
+  // memory (the two together may not exceed the per-block limit).
+  if (smem > 48 * 1024) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, f) != cudaSuccess ||
+        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dev.smem_optin - static_cast<int>(fa.sharedSizeBytes)) != cudaSuccess)
+      return -1;
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, threads, smem) != cudaSuccess) return -1;
   std::lock_guard<std::mutex> g(g_mu);

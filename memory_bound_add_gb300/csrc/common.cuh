@@ -432,12 +432,14 @@ __device__ __forceinline__ Part merge(const Part& a, const Part& b) {
   const float d = b.m - a.m;  // squared below, so its sign does not matter
   o.n = a.n + b.n;
   if constexpr (EQUAL) {
-    o.m = (a.m + b.m) * 0.5f;
-    o.M2 = fmaf(d * d, a.n * 0.5f, a.M2 + b.M2);
+    o.m = __fmul_rn(__fadd_rn(a.m, b.m), 0.5f);
+    o.M2 = fmaf(__fmul_rn(d, d), __fmul_rn(a.n, 0.5f), __fadd_rn(a.M2, b.M2));
   } else {
+    // explicit roundings: a multiply-add the compiler contracted into one
+    // fma would round the two sides differently and break the symmetry
     const float inv = __frcp_rn(fmaxf(o.n, 1.0f));
-    o.m = (a.n * a.m + b.n * b.m) * inv;
-    o.M2 = fmaf(d * d, (a.n * b.n) * inv, a.M2 + b.M2);
+    o.m = __fmul_rn(__fadd_rn(__fmul_rn(a.n, a.m), __fmul_rn(b.n, b.m)), inv);
+    o.M2 = fmaf(__fmul_rn(d, d), __fmul_rn(__fmul_rn(a.n, b.n), inv), __fadd_rn(a.M2, b.M2));
   }
   return o;
 }

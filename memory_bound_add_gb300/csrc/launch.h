@@ -41,6 +41,7 @@ struct LaunchCtx {
   bool pdl;          // launch with programmatic stream serialisation
   int cta_threads;   // CTA-per-row kernels: threads per CTA, 0 = by H
   int stages;        // TMA path: rows staged per CTA, 0 = by shared memory
+  int warp_rows = 0; // warp-per-row vector path: rows a warp takes, 0 = by shape
 };
 
 // Each launcher returns 0, or ADDLN_ERR_UNSUPPORTED when its kernel family

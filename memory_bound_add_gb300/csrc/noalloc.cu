@@ -18,11 +18,12 @@
 // device gets a new context and the address is looked up again); that first
 // call on a device should therefore come before any stream capture.  Nothing
 // here allocates: the call forwards to add_layernorm_bwd with the buffer as
-// its workspace, so it runs exactly the same kernels.  Every CTA writes all of its [2][H] partial before the
-// column-sum kernel reads it, so no part of the buffer has to start at zero;
-// the buffer keeps whatever the last call left.  All calls on a device share
-// the one buffer: calls that can overlap on the GPU (other streams, other host
-// threads) race on it and must be serialised by the caller.
+// its workspace, so it runs exactly the same kernels.  Every CTA writes all
+// of its [2][H] partial before the column-sum kernel reads it, so no part of
+// the buffer has to start at zero; the buffer keeps whatever the last call
+// left.  All calls on a device share the one buffer: calls that can overlap
+// on the GPU (other streams, other host threads) race on it and must be
+// serialised by the caller.
 #include <mutex>
 
 #include <cuda_runtime.h>

@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(THREADS) k_cta_scalar(const RowArgs p) {
   int64_t it = 0;
   for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
     const int64_t base = row * static_cast<int64_t>(H);
-    constexpr int S = IO::kBytes;
+    [[maybe_unused]] constexpr int S = IO::kBytes;  // used by the checked build's tests
     float K = 0.f;
     if (ADDLN_IN(221, base * S, S, rows_bytes(p, S)))
       K = has_r ? IO::load1(p.x, base) + IO::load1(p.r, base) : IO::load1(p.x, base);
@@ -442,10 +442,15 @@ int resident_ctas(const void* f, int threads, int smem, const DeviceInfo& dev) {
   }
   // The limit is per function: raise it once to the device's opt-in maximum
   // (never to this launch's size, which a later, larger launch would exceed).
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin) !=
-          cudaSuccess)
-    return -1;
+  // Raised to the device's opt-in maximum less the kernel's static shared
+  // memory (the two together may not exceed the per-block limit).
+  if (smem > 48 * 1024) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, f) != cudaSuccess ||
+        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dev.smem_optin - static_cast<int>(fa.sharedSizeBytes)) != cudaSuccess)
+      return -1;
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, threads, smem) != cudaSuccess) return -1;
   std::lock_guard<std::mutex> g(g_occ_mu);

@@ -54,7 +54,9 @@ __device__ __forceinline__ float rescale(float from, float to) {
 __device__ __forceinline__ SPart merge(const SPart& a, const SPart& b) {
   SPart o;
   o.m = fmaxf(a.m, b.m);
-  o.s = a.s * rescale(a.m, o.m) + b.s * rescale(b.m, o.m);
+  // explicit roundings keep merge(a, b) and merge(b, a) bitwise equal (a
+  // contracted multiply-add would round the two sides differently)
+  o.s = __fadd_rn(__fmul_rn(a.s, rescale(a.m, o.m)), __fmul_rn(b.s, rescale(b.m, o.m)));
   return o;
 }
 
@@ -529,10 +531,15 @@ int resident(const void* f, int threads, int smem, const DeviceInfo& dev) {
   }
   // The limit is per function: raise it once to the device's opt-in maximum
   // (never to this launch's size, which a later, larger launch would exceed).
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin) !=
-          cudaSuccess)
-    return -1;
+  // Raised to the device's opt-in maximum less the kernel's static shared
+  // memory (the two together may not exceed the per-block limit).
+  if (smem > 48 * 1024) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, f) != cudaSuccess ||
+        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dev.smem_optin - static_cast<int>(fa.sharedSizeBytes)) != cudaSuccess)
+      return -1;
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, threads, smem) != cudaSuccess) return -1;
   std::lock_guard<std::mutex> g(g_mu);

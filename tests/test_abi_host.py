@@ -51,7 +51,8 @@ def test_header_declares_the_expected_entry_points():
         "addln_strerror",
         "addln_max_hidden", "addln_bounds_checked", "addln_bounds_violation",
         "addln_get_device_error", "addln_set_force_path", "addln_set_wait_limit_ns",
-        "addln_set_grid_cap", "addln_set_pdl", "addln_set_cta_shape", "addln_last_path",
+        "addln_set_grid_cap", "addln_set_pdl", "addln_set_cta_shape", "addln_set_warp_rows",
+        "addln_last_path",
         "addln_last_cuda_error"])
 
 

@@ -129,10 +129,14 @@ def test_workspace_errors_and_zero_rows():
     db = torch.empty(w.H, device="cuda")
     need = mba.add_layernorm_bwd_workspace_size(64, w.H, mba.FP16)
     assert need > 0
-    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    # the size covers every plan the pointers may pick (vector or element
+    # path); one partial of [2][H] floats is less than any plan needs
+    small = torch.empty(8 * w.H, dtype=torch.uint8, device="cuda")
     with pytest.raises(mba.AddLNError) as e:
         mba.add_layernorm_bwd(dy, a, mean, rstd, gamma, dx, dg, db, workspace=small)
     assert e.value.code == mba.binding.ERR_WORKSPACE
+    enough = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    mba.add_layernorm_bwd(dy, a, mean, rstd, gamma, dx, dg, db, workspace=enough)
     # no dgamma / dbeta: no workspace needed
     mba.add_layernorm_bwd(dy, a, mean, rstd, gamma, dx)
     dg.fill_(7.0)
@@ -167,3 +171,25 @@ def test_wait_timeout_sets_device_error_and_recovers():
     assert mba.addln_get_device_error() == 0
     out, p = run(case)
     check(case, w.dtype, out, "after timeout")
+
+
+def test_workspace_reused_across_calls_and_shapes():
+    # one workspace, large enough for the largest shape, serves calls of
+    # several shapes in a row, each result matching the oracle
+    shapes = [("pages_2048x4096_fp16", 700), ("bert_base_4096x768_fp16", 900),
+              ("large_32768x8192_bf16", 200), ("pages_2048x4096_fp16", 33)]
+    need = max(mba.add_layernorm_bwd_workspace_size(r, synth.get(n).H,
+                                                    mba.binding.DTYPE_CODE[TD[synth.get(n).dtype]])
+               for n, r in shapes)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    for name, rows in shapes * 2:
+        w = synth.with_rows(synth.get(name), rows)
+        case = make_case(w, seed=rows)
+        dy, a, mean, rstd, gamma, _ = [t.cuda() if t is not None else None for t in case]
+        dx = torch.empty_like(dy)
+        dg = torch.empty(w.H, device="cuda")
+        db = torch.empty(w.H, device="cuda")
+        mba.add_layernorm_bwd(dy, a, mean, rstd, gamma, dx, dg, db, workspace=ws)
+        torch.cuda.synchronize()
+        assert mba.addln_get_device_error() == 0
+        check(case, w.dtype, (dx.cpu(), dg.cpu(), db.cpu()), f"{name} {rows} shared workspace")

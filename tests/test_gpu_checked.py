@@ -5,8 +5,12 @@ buffers and capped persistent grids, through the checked library's own C ABI.
 In that build each global load, store, bulk copy and L2 prefetch is first
 tested against its buffer's extent; an access that would leave its buffer is
 skipped and reported as ADDLN_ERR_BOUNDS.  Every call here must report none,
-and since the tests change no arithmetic, every output must equal the normal
-library's bit for bit."""
+and every output must agree with the normal library's: the tests change no
+arithmetic, but the two builds may contract a multiply and an add
+differently, and the backward's grid (hence how its column partials are
+grouped) follows each build's occupancy, so values agree to a couple of fp32
+roundings (outputs an access skipped would be far off: zeros or stale
+memory)."""
 from __future__ import annotations
 
 import ctypes
@@ -46,6 +50,16 @@ def S():
 def no_violation(lib, what):
     rc = lib.addln_get_device_error(S())
     assert rc == 0, f"{what}: {lib.addln_strerror(rc).decode()} (word {lib.addln_bounds_violation():#x})"
+
+
+def assert_close(u, v, what):
+    """Within two units in the last place of the output dtype (fp32: 2^-22
+    relative) of the larger magnitude, plus 1e-6 absolute."""
+    a, b = u.double(), v.double()
+    rel = {torch.float32: 2.0 ** -22, torch.float16: 2.0 ** -10, torch.bfloat16: 2.0 ** -7}[u.dtype]
+    bound = rel * torch.maximum(a.abs(), b.abs()) + 1e-6
+    bad = ~((a - b).abs() <= bound)
+    assert not bad.any(), f"{what}: {int(bad.sum())} values differ, e.g. {a[bad][:3]} vs {b[bad][:3]}"
 
 
 def misaligned_copy(t):
@@ -89,7 +103,7 @@ def test_forward(chk, rows, H, dtype, path, cap):
             no_violation(lib, f"forward {rows}x{H} {dtype} path {path} cap {cap}")
         outs[tag] = (y, a, m, s)
     for u, v in zip(outs["normal"], outs["checked"]):
-        assert torch.equal(u, v)
+        assert_close(u, v, f"forward {rows}x{H} {dtype} path {path}")
 
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16", "fp32"])
@@ -111,7 +125,7 @@ def test_softmax(chk, dtype, H, path):
         torch.cuda.synchronize()
         ys.append(y)
     no_violation(chk, f"softmax {rows}x{H} {dtype} path {path}")
-    assert torch.equal(ys[0], ys[1])
+    assert_close(ys[0], ys[1], f"softmax {rows}x{H} {dtype}")
 
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16", "fp32"])
@@ -137,7 +151,7 @@ def test_elementwise(chk, dtype, H, aligned):
         res.append((y, t, u, a))
     no_violation(chk, f"elementwise {rows}x{H} {dtype} aligned={aligned}")
     for u, v in zip(*res):
-        assert torch.equal(u, v)
+        assert_close(u, v, f"elementwise {rows}x{H} {dtype}")
 
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16", "fp32"])
@@ -171,5 +185,9 @@ def test_backward(chk, dtype, H, scalar, with_dres):
         torch.cuda.synchronize()
         res.append((dx, dg, db))
     no_violation(chk, f"backward {rows}x{H} {dtype} scalar={scalar} dres={with_dres}")
-    for u, v in zip(*res):
-        assert torch.equal(u, v)
+    assert_close(res[0][0], res[1][0], f"backward dx {rows}x{H} {dtype}")
+    # column sums: partials grouped as each build's grid falls, so within
+    # 1e-5 of the sum of magnitudes over the rows
+    mag = (dy.double().abs().sum(0) * 4).float()
+    for u, v in zip(res[0][1:], res[1][1:]):
+        assert ((u - v).abs() <= 1e-5 * mag + 1e-6).all(), f"backward columns {rows}x{H} {dtype}"

@@ -461,6 +461,26 @@ def test_dependent_chain_keeps_order_under_pdl(name):
     assert_correctly_rounded(results[1][0], ref[0], w.dtype, f"{name} chain layer 0")
 
 
+@pytest.mark.parametrize("warp_rows", [1, 2])
+@pytest.mark.parametrize("name,rows", [("bert_base_4096x768_fp16", 777), ("cancel_65536x1000_bf16", 1201),
+                                       ("tiny_64x768_fp32", 63), ("bert_base_4096x768_fp16", 1)])
+@pytest.mark.parametrize("want_a,want_stats", [(False, False), (True, True)])
+def test_rows_per_warp(name, rows, warp_rows, want_a, want_stats):
+    # one or two rows a warp on the warp-per-row vector path; an odd row
+    # count leaves the last warp a single live row
+    w = synth.with_rows(synth.get(name), rows)
+    d = synth.make_inputs(w, seed=15 + rows)
+    prev = mba.addln_set_warp_rows(warp_rows)
+    try:
+        out = run_fused(d, 0, want_a=want_a, want_stats=want_stats)
+    finally:
+        mba.addln_set_warp_rows(prev)
+    nv = (w.H // (4 if w.dtype == "fp32" else 8) + 31) // 32
+    two = warp_rows == 2 and nv in (3, 4)
+    assert out["path"].startswith("warp_vec2" if two else "warp_vec_"), out["path"]
+    check(w, d, out, f"{name} x{rows} warp_rows={warp_rows} {out['path']}")
+
+
 @pytest.mark.parametrize("threads", [128, 256, 512])
 @pytest.mark.parametrize("stages", [1, 2, 3, 4])
 def test_tma_tuning_shapes(threads, stages):
