@@ -348,6 +348,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// L2 policy of ordinary priority (a bulk copy given no hint gets the same).
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // Tests phase `parity`; if it is not complete the thread may be suspended
 // (not spinning, so it takes no issue slots) until the phase completes or
 // about suspend_ns nanoseconds pass.

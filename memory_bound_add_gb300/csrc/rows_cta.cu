@@ -157,7 +157,11 @@ __global__ void __launch_bounds__(THREADS) __maxnreg__((cta_row_max_regs<DT, THR
       fence_mbar_init();
     }
     __syncthreads();
-    policy = policy_evict_first();
+    // Ordinary L2 priority for the staged rows.  Marking them evict-first
+    // (they are read once) measured slower back to back: 2048 x 4096 fp16
+    // 8.81 us a step against 7.90, 2048 x 8192 bf16 21.9 against 21.0, the
+    // same at 32768 x 8192 (DRAM bytes a launch unchanged).
+    policy = policy_evict_normal();
   }
   pdl_trigger();
   pdl_wait();  // the previous kernel's writes are visible from here on
