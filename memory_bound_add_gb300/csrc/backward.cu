@@ -12,8 +12,9 @@
 // thread always handles the same columns, so it accumulates its columns'
 // dgamma / dbeta contributions in its own shared-memory slots (no races, no
 // atomics); at the end every CTA writes one [2][H] partial to the caller's
-// workspace, and k_colsum adds the G partials of each column in a fixed
-// order.  The result is bitwise deterministic.
+// workspace, and a second kernel (k_colsum4 for even H, k_colsum otherwise)
+// adds the G partials of each column in a fixed order.  The result is bitwise
+// deterministic.
 //
 // Shapes: one warp per row (4 warps per CTA, 16-byte vectors) for H <= 1024;
 // one CTA per row with dY and A staged by TMA bulk copies on a bounded
@@ -650,6 +651,89 @@ __global__ void __launch_bounds__(kColCols * SLICES, 32 / SLICES) k_colsum(const
   }
 }
 
+// The same sums for even H, where every partial's columns can be read 16
+// bytes at a time.  A block covers 4·QUADS adjacent columns (QUADS column
+// quads of every partial); thread t takes quad t % QUADS and the partials
+// o, o + T/QUADS, o + 2T/QUADS, ... (o = t / QUADS), issues the loads of up
+// to eight of them at once and adds them in that order; the sums of a quad
+// are then added by a butterfly over the warp's lanes of that quad (every
+// lane ends with the same value) and across the warps in warp order.  The
+// order depends only on G, H, QUADS and T, never on scheduling.  Every load
+// of a thread is in flight at once: the partials sit in L2, and the
+// kernel's time is its latency.
+constexpr int kCol4Threads = 256;
+
+// Quads a block: the most (of 2, 4, 8) whose G loads a column quad still
+// fit in one round of eight loads a thread.  Wider blocks mean fewer of
+// them; a second round of L2 latency costs more than the extra blocks.
+// (µs a step, backward with these sums, 2 / 4 / 8 quads: 2048×4096 fp16,
+// G = 304: 17.31 / 15.87 / 17.19; 4096×768 fp16, G = 608: 11.67 / 13.40 /
+// 16.18; 32768×8192 bf16, G = 152: 273.4 / 271.6 / 271.1.)
+inline int colsum_quads(int64_t G) {
+  constexpr int64_t kOneRound = 8 * kCol4Threads;  // loads a block issues in one round
+  if (8 * G <= kOneRound) return 8;
+  if (4 * G <= kOneRound) return 4;
+  return 2;
+}
+
+template <int QUADS>
+__global__ void __launch_bounds__(kCol4Threads) k_colsum4(const float* ws, int64_t G, int H,
+                                                         float* dgamma, float* dbeta) {
+  static_assert(QUADS >= 1 && QUADS <= 32 && (QUADS & (QUADS - 1)) == 0, "quads: a power of two");
+  constexpr int NW = kCol4Threads / 32;
+  constexpr int64_t kStep = kCol4Threads / QUADS;  // partials between a thread's loads
+  constexpr int kU = 8;                            // loads in flight a thread
+  __shared__ float4 wsum[NW][QUADS];
+  pdl_trigger();
+  pdl_wait();
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, q = t % QUADS;
+  const int64_t ld = 2 * static_cast<int64_t>(H);
+  const int64_t j = (static_cast<int64_t>(blockIdx.x) * QUADS + q) * 4;  // the thread's first column
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (j < ld) {
+    for (int64_t b0 = t / QUADS; b0 < G; b0 += kStep * kU) {
+      float4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int64_t b = b0 + u * kStep;
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (b < G && ADDLN_IN(633, (b * ld + j) * 4, 16, G * ld * 4))
+          v[u] = __ldcg(reinterpret_cast<const float4*>(ws + b * ld + j));
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
+      }
+    }
+  }
+#pragma unroll
+  for (int off = QUADS; off < 32; off <<= 1) {
+    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+  }
+  if (lane < QUADS) wsum[warp][lane] = acc;
+  __syncthreads();
+  if (t < QUADS && j < ld) {
+    float4 r = wsum[0][t];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) {
+      const float4 u = wsum[w][t];
+      r.x += u.x; r.y += u.y; r.z += u.z; r.w += u.w;
+    }
+    const float e[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t c = j + k;
+      if (c < H)
+        dgamma[c] = e[k];
+      else if (c < ld && ADDLN_IN(634, 4 * (c - H), 4, 4 * static_cast<int64_t>(H)))
+        dbeta[c - H] = e[k];
+    }
+  }
+}
+
 // ------------------------------------------------------------------ host
 namespace {
 
@@ -868,7 +952,19 @@ int launch_bwd(int dtype, const void* dy, const void* a, const float* mean, cons
     note_cuda_error(static_cast<int>(e));
     return ADDLN_ERR_LAUNCH;
   }
-  if (want_cols) {
+  if (want_cols && H % 2 == 0) {
+    // 16-byte reads of the partials: 2H is a multiple of 4 and the
+    // workspace is 16-byte aligned
+    const int quads = bw::colsum_quads(partials);
+    const int64_t blocks = (2 * H / 4 + quads - 1) / quads;
+    auto k = quads == 2 ? bw::k_colsum4<2> : quads == 4 ? bw::k_colsum4<4> : bw::k_colsum4<8>;
+    e = launch_kernel(k, dim3(static_cast<unsigned>(blocks)), dim3(bw::kCol4Threads), 0, c.stream, c.pdl,
+                      static_cast<const float*>(ws), partials, static_cast<int>(H), dgamma, dbeta);
+    if (e != cudaSuccess) {
+      note_cuda_error(static_cast<int>(e));
+      return ADDLN_ERR_LAUNCH;
+    }
+  } else if (want_cols) {
     const int64_t cols = 2 * H;
     const int64_t blocks = (cols + bw::kColCols - 1) / bw::kColCols;
     if (blocks < c.dev.sms)
