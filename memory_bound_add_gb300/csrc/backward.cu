@@ -810,16 +810,20 @@ int plan_cta(const BwdArgs& p, const DeviceInfo& dev, Plan* pl) {
   return ADDLN_OK;
 }
 
-// Register-resident kernel: two ring slots a warp by default (three for the
-// warp-per-row form, which holds a slot for its whole row); the slot knob
-// (1..4) changes only the launch's slots, never its grid, so the workspace
-// size does not depend on it.  The warp-per-row form keeps at least two
-// slots, whose space its final per-warp column sums reuse.
+// Register-resident kernel: two ring slots a warp by default, three for
+// 512-thread CTAs (one to an SM, so fewer rows in flight an SM otherwise).
+// Measured, µs a step at 2 / 3 / 4 slots: 4096x768 fp16 (warp per row)
+// 11.37 / 11.57 / 12.59; 65536x1000 bf16 (warp per row) 69.9 / 70.5 / 75.5;
+// 2048x4096 fp16 (256 threads) 15.97 / 16.08 / 16.28; 32768x8192 bf16
+// (512 threads) 270.3 / 267.9 / 268.2.  The slot knob (1..4) changes only
+// the launch's slots, never its grid, so the workspace size does not depend
+// on it.  The warp-per-row form keeps at least two slots, whose space its
+// final per-warp column sums reuse.
 template <int DT, int THREADS, int NV, bool FULL, bool ROWWARP>
 int plan_res(const BwdArgs& p, const DeviceInfo& dev, int stages_knob, Plan* pl) {
   constexpr int NW = THREADS / 32;
   constexpr uint32_t region = 2u * 32u * NV * 16u;
-  constexpr int kDefaultStages = ROWWARP ? 3 : 2;
+  constexpr int kDefaultStages = !ROWWARP && THREADS >= 512 ? 3 : 2;
   auto smem_of = [](int st) {
     return static_cast<uint32_t>(st) * NW * region + 8u * kMaxStagesRes * NW + 2u * NW * 8u;
   };
