@@ -173,6 +173,23 @@ def test_wait_timeout_sets_device_error_and_recovers():
     check(case, w.dtype, out, "after timeout")
 
 
+@pytest.mark.parametrize("rows,H,dtype,min_g,max_g", [
+    (16384, 64, "fp32", 1025, None),   # more than 1024 partials: two rounds of loads a thread
+    (4096, 768, "bf16", 513, 1024),    # two column quads a block, one round
+    (2048, 4096, "fp16", 257, 512),    # four quads a block
+    (512, 8192, "bf16", 1, 256),       # eight quads a block
+])
+def test_column_sum_widths(rows, H, dtype, min_g, max_g):
+    # the column-sum kernel picks its block width from the number of
+    # partials G (= workspace bytes / 8H); each case sits in one band of G
+    w = synth.custom(rows, H, dtype)
+    g_count = mba.add_layernorm_bwd_workspace_size(rows, H, mba.binding.DTYPE_CODE[TD[dtype]]) // (8 * H)
+    assert g_count >= min_g and (max_g is None or g_count <= max_g), g_count
+    case = make_case(w, seed=rows + H)
+    out, p = run(case)
+    check(case, w.dtype, out, f"{rows}x{H} {dtype} G={g_count} {p}")
+
+
 def test_workspace_reused_across_calls_and_shapes():
     # one workspace, large enough for the largest shape, serves calls of
     # several shapes in a row, each result matching the oracle
