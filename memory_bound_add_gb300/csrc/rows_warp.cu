@@ -14,8 +14,12 @@
 
 namespace addln {
 
-constexpr int kWarpCtaThreads = 128;  // 4 rows per CTA
-constexpr int kRowsPerCta = kWarpCtaThreads / 32;
+// Four warps a CTA; one warp a CTA when four-warp CTAs would leave SMs
+// without work (a launch of fewer than 4 x SMs warps' rows): then the rows
+// spread over as many SMs as there are warps (64x768 fp32: 2.15 -> 1.95 us a
+// step; at 4096x768 fp16 one-warp CTAs measured slower, 4.31 against 4.11,
+// and two-warp CTAs level).  The kernels take the warps a CTA from blockDim.
+constexpr int kWarpCtaThreads = 128;
 
 // Register cap a lane: 64 while it holds at most 24 values in at most four
 // vectors (eight 128-thread CTAs to an SM); 72 for fp32 rows of six vectors,
@@ -50,7 +54,7 @@ __global__ void __launch_bounds__(kWarpCtaThreads)
   constexpr int S = IO::kBytes;
   const int lane = threadIdx.x & 31;
   const int64_t row0 =
-      (static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5)) * RPW;
+      (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW;
   const int H = p.H;
   // while the previous kernel may still be finishing, ask L2 for this warp's
   // rows of X and R (a hint only: nothing is read before the wait below, and
@@ -196,7 +200,7 @@ template <int DT, int NV, bool FULL>
 __global__ void __launch_bounds__(kWarpCtaThreads, 2) k_warp_row(const RowArgs p) {
   using IO = Io<DT>;
   const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   pdl_trigger();
   pdl_wait();
   if (row >= p.rows) return;  // whole warp leaves together
@@ -263,18 +267,20 @@ __global__ void __launch_bounds__(kWarpCtaThreads, 2) k_warp_row(const RowArgs p
 
 template <int DT, int NV, bool VECTOR, int RPW = 1>
 static int launch(const RowArgs& p, const LaunchCtx& c) {
-  const int64_t blocks = (p.rows + kRowsPerCta * RPW - 1) / (kRowsPerCta * RPW);
+  const int64_t rows_per_cta4 = static_cast<int64_t>(kWarpCtaThreads / 32) * RPW;
+  const int warps = (p.rows + rows_per_cta4 - 1) / rows_per_cta4 < c.dev.sms ? 1 : kWarpCtaThreads / 32;
+  const int64_t blocks = (p.rows + warps * RPW - 1) / (warps * RPW);
   if (blocks > 0x7fffffff) return ADDLN_ERR_UNSUPPORTED;
   constexpr int VEC = VECTOR ? Io<DT>::kVec : 1;
   const bool full = (p.H / VEC) == 32 * NV;
   const dim3 grid(static_cast<unsigned>(blocks));
   cudaError_t e;
   if constexpr (VECTOR)
-    e = full ? launch_kernel(k_warp_row_vec<DT, NV, true, RPW>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p)
-             : launch_kernel(k_warp_row_vec<DT, NV, false, RPW>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p);
+    e = full ? launch_kernel(k_warp_row_vec<DT, NV, true, RPW>, grid, dim3(32 * warps), 0, c.stream, c.pdl, p)
+             : launch_kernel(k_warp_row_vec<DT, NV, false, RPW>, grid, dim3(32 * warps), 0, c.stream, c.pdl, p);
   else
-    e = full ? launch_kernel(k_warp_row<DT, NV, true>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p)
-             : launch_kernel(k_warp_row<DT, NV, false>, grid, dim3(kWarpCtaThreads), 0, c.stream, c.pdl, p);
+    e = full ? launch_kernel(k_warp_row<DT, NV, true>, grid, dim3(32 * warps), 0, c.stream, c.pdl, p)
+             : launch_kernel(k_warp_row<DT, NV, false>, grid, dim3(32 * warps), 0, c.stream, c.pdl, p);
   if (e != cudaSuccess) note_cuda_error(static_cast<int>(e));
   return e == cudaSuccess ? ADDLN_OK : ADDLN_ERR_LAUNCH;
 }
