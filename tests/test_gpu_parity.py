@@ -481,6 +481,24 @@ def test_rows_per_warp(name, rows, warp_rows, want_a, want_stats):
     check(w, d, out, f"{name} x{rows} warp_rows={warp_rows} {out['path']}")
 
 
+@pytest.mark.parametrize("offset", [-5, -1, 0, 3])
+@pytest.mark.parametrize("warp_rows", [1, 2])
+def test_warp_cta_size_switch(offset, warp_rows):
+    # the warp-per-row kernels take one-warp CTAs while four-warp CTAs
+    # would be fewer than the SMs (rows < 4 x SMs x rows-a-warp), four-warp
+    # CTAs from there on: both sides of the switch and the rows at it
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = 4 * sms * warp_rows + offset
+    w = synth.with_rows(synth.get("bert_base_4096x768_fp16"), rows)
+    d = synth.make_inputs(w, seed=21 + rows)
+    prev = mba.addln_set_warp_rows(warp_rows)
+    try:
+        out = run_fused(d, 0, want_a=True, want_stats=True)
+    finally:
+        mba.addln_set_warp_rows(prev)
+    check(w, d, out, f"bert x{rows} warp_rows={warp_rows} {out['path']}")
+
+
 @pytest.mark.parametrize("threads", [128, 256, 512])
 @pytest.mark.parametrize("stages", [1, 2, 3, 4])
 def test_tma_tuning_shapes(threads, stages):
