@@ -360,6 +360,28 @@ def test_full_size_every_row(name):
         assert torch.equal(out["y"][i], d["beta"].to(TD[w.dtype]))
 
 
+@pytest.mark.parametrize("name,rows", [("tiny_64x768_fp32", 64), ("bert_base_4096x768_fp16", 3000),
+                                       ("pages_2048x4096_fp16", 64), ("tail_4096x999_bf16", 40)])
+@pytest.mark.parametrize("path", ["auto", "cta_vec", "scalar"])
+def test_nan_and_inf_stay_in_their_row(name, rows, path):
+    # a NaN in one row of X and an infinity in another row of R make those
+    # rows' Y NaN (the definition's mean and variance are NaN there) and
+    # leave every other row as the oracle computes it; rows 0 and 1 share a
+    # warp on the two-rows-a-warp path
+    w = synth.with_rows(synth.get(name), rows)
+    if not _supported(path, w):
+        pytest.skip("path does not take this shape")
+    d = synth.make_inputs(w, seed=16 + rows)
+    d["x"][0, w.H // 3] = float("nan")
+    d["r"][rows - 1, w.H - 1] = float("inf")
+    out = run_fused(d, PATHS[path], want_a=True, want_stats=True)
+    for i in (0, rows - 1):
+        assert torch.isnan(out["y"][i]).all(), (i, out["path"])
+        assert torch.isnan(out["mean"][i]) or torch.isinf(out["mean"][i]), (i, out["path"])
+    keep = np.arange(1, rows - 1)
+    check(w, d, out, f"{name} x{rows} NaN/inf rows {out['path']}", rows=keep)
+
+
 @pytest.mark.parametrize("H", [768, 4096])
 def test_eps_zero_constant_row_is_nan_like_the_definition(H):
     # eps = 0 is accepted: a constant row is 0/0 (NaN Y, rstd = inf, the mean
