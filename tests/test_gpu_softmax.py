@@ -75,6 +75,22 @@ def test_small_all_paths(name, path):
     check(d["x"], w.dtype, y, f"{name}/{path}/{p}")
 
 
+@pytest.mark.parametrize("name", synth.SOFTMAX_NAMES)
+@pytest.mark.parametrize("path", list(PATHS))
+def test_nan_stays_in_its_row(name, path):
+    # a NaN in one row makes that row's y NaN (its maximum and sum are NaN)
+    # and leaves the neighbouring rows as the oracle computes them
+    w = synth.with_rows(synth.get(name), 37)
+    if not _ok(path, w.H, w.dtype):
+        pytest.skip("path cannot run this row layout")
+    d = synth.make_inputs(w, seed=9)
+    d["x"][5, w.H // 2] = float("nan")
+    y, p = run(d["x"], PATHS[path])
+    assert torch.isnan(y[5]).all(), p
+    keep = np.array([i for i in range(37) if i != 5])
+    check(d["x"], w.dtype, y, f"{name}/{path}/{p} NaN row", rows=keep)
+
+
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
 @pytest.mark.parametrize("H", [1, 2, 7, 8, 33, 257, 1000, 1024, 1025, 4096, 4097, 12288, 32000])
 def test_shape_sweep(dtype, H):
