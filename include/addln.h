@@ -225,7 +225,10 @@ int gelu_fwd(const void *t, void *u, int64_t n, int dtype, void *stream);
  *   workspace  device scratch of at least add_layernorm_bwd_workspace_size()
  *              bytes, 16-byte aligned, owned by the caller; needed only with
  *              dgamma / dbeta.  Holds per-CTA column partials, summed in a
- *              fixed order, so the results are bitwise reproducible.  Its
+ *              fixed order, so the results are bitwise reproducible from
+ *              call to call for a shape on one GPU model (the number of
+ *              partials follows the SM count and occupancy, so another
+ *              model may round the sums differently).  Its
  *              contents need no initialisation; calls that may overlap on
  *              the GPU must not share a workspace.
  * rows == 0 zero-fills dgamma and dbeta.  fp32 arithmetic; dx rounded to
