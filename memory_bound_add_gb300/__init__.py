@@ -39,4 +39,4 @@ from .binding import (  # noqa: F401
     FP32, FP16, BF16,
     PATH_AUTO, PATH_WARP_VEC, PATH_CTA_TMA, PATH_CTA_VEC, PATH_SCALAR,
 )
-from .autograd import AddLayerNormFunction, add_layernorm_train  # noqa: F401
+from .autograd import AddLayerNormFunction, FusedAddLayerNorm, add_layernorm_train  # noqa: F401

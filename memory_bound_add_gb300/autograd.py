@@ -50,3 +50,18 @@ class AddLayerNormFunction(torch.autograd.Function):
 def add_layernorm_train(x, r, gamma, beta, eps: float = 1e-5):
     """The fused Add + LayerNorm with gradients for x, r, gamma and beta."""
     return AddLayerNormFunction.apply(x, r, gamma, beta, eps)
+
+
+class FusedAddLayerNorm(torch.nn.Module):
+    """LayerNorm(x + r) over the last dimension as one module: learnable fp32
+    gamma (ones) and beta (zeros) of size H, forward and backward in the
+    library's kernels."""
+
+    def __init__(self, hidden: int, eps: float = 1e-5, device=None):
+        super().__init__()
+        self.eps = float(eps)
+        self.weight = torch.nn.Parameter(torch.ones(hidden, dtype=torch.float32, device=device))
+        self.bias = torch.nn.Parameter(torch.zeros(hidden, dtype=torch.float32, device=device))
+
+    def forward(self, x, r):
+        return AddLayerNormFunction.apply(x, r, self.weight, self.bias, self.eps)

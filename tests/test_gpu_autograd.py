@@ -72,3 +72,24 @@ def test_only_some_inputs_need_gradients():
     torch.cuda.synchronize()
     assert x.grad is not None and r2.grad is not None and g2.grad is not None
     assert torch.equal(x.grad, r2.grad)
+
+
+def test_module_trains():
+    # the module's parameters get gradients and an optimizer step moves them;
+    # its output equals the function's with the same parameters
+    w = synth.with_rows(synth.get("bert_base_4096x768_fp16"), 64)
+    d = synth.make_inputs(w, seed=35)
+    m = mba.FusedAddLayerNorm(w.H, eps=d["eps"], device="cuda")
+    with torch.no_grad():
+        m.weight.copy_(d["gamma"].cuda())
+        m.bias.copy_(d["beta"].cuda())
+    x, r = d["x"].cuda(), d["r"].cuda()
+    y = m(x, r)
+    assert torch.equal(y, mba.add_layernorm(x, r, m.weight.detach(), m.bias.detach(), eps=d["eps"])[0])
+    opt = torch.optim.SGD(m.parameters(), lr=0.1)
+    before = m.weight.detach().clone()
+    y.float().square().mean().backward()
+    opt.step()
+    torch.cuda.synchronize()
+    assert m.weight.grad is not None and m.bias.grad is not None
+    assert not torch.equal(before, m.weight.detach())
